@@ -1,0 +1,151 @@
+// oneshot.cu -- one-shot AllReduce over N virtual ranks: every rank reads all
+// peers' inputs and reduces them itself.
+//
+// Pages cited (by title, then section):
+//   [OS89] "perf(osar): all-reduce 5커널 → 3커널 (가드·웨이트 프롤로그 융합) - #89"
+//          (the one-shot kernel: each rank copies in, then reduces all peers)
+//   [NOTES] "NCCL" notes (cishoon.github.io), section "5 Symmetric Memory" (a
+//          rank reads a peer's buffer by pointer; one kernel, one hop)
+//
+// On one GPU the ranks' buffers are already addressable by pointer, so the
+// copy-in / signal / wait stages of the page's kernel have nothing to move or
+// wait for: each rank's blocks read the N inputs directly. Block b serves
+// rank b % N and tile b / N; the N blocks of a tile are adjacent in launch
+// order, so they run together and the N-fold reads of one input tile are
+// served mostly from L2.
+//
+// Sum: binary32, in user-rank order 0..N-1, starting from x_0 (no added
+// zero), rounded once to bf16 for bf16 data.
+#include "rar_launch.h"
+
+namespace rar {
+
+constexpr int kOneShotThreads = 256;
+constexpr int kOneShotUnroll = 2;
+
+template <typename T>
+struct OsPack;
+template <>
+struct OsPack<float> {
+  static constexpr int kElems = 4;
+  __device__ static __forceinline__ void widen(uint4 u, float (&v)[8]) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
+  }
+  __device__ static __forceinline__ uint4 narrow(const float (&v)[8]) {
+    return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+  }
+};
+template <>
+struct OsPack<uint16_t> {
+  static constexpr int kElems = 8;
+  __device__ static __forceinline__ void widen(uint4 u, float (&v)[8]) {
+    v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+    v[4] = bf16lo(u.z); v[5] = bf16hi(u.z); v[6] = bf16lo(u.w); v[7] = bf16hi(u.w);
+  }
+  __device__ static __forceinline__ uint4 narrow(const float (&v)[8]) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ float os_scalar(const T* p);
+template <>
+__device__ __forceinline__ float os_scalar<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float os_scalar<uint16_t>(const uint16_t* p) { return __uint_as_float((uint32_t)*p << 16); }
+template <typename T>
+__device__ __forceinline__ void os_store_scalar(T* p, float v);
+template <>
+__device__ __forceinline__ void os_store_scalar<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void os_store_scalar<uint16_t>(uint16_t* p, float v) {
+  __nv_bfloat16 b = __float2bfloat16_rn(v);
+  *p = *reinterpret_cast<uint16_t*>(&b);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_constant__ OneShotArgs a) {
+  constexpr int P = OsPack<T>::kElems;
+  constexpr int U = kOneShotUnroll;
+  const int N = a.nranks;
+  const int rank = blockIdx.x % N;
+  const int64_t tile = blockIdx.x / N;
+  const int64_t ntiles = gridDim.x / N;
+  const int64_t npack = a.count / P;
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
+  const int64_t per_tile = (int64_t)kOneShotThreads * U;
+  for (int64_t base = tile * per_tile; base < npack; base += ntiles * per_tile) {
+    float acc[U][8];
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+      if (p < npack) {
+        w[u] = ld_stream_v4(reinterpret_cast<const T*>(a.send[0]) + p * P);
+        OsPack<T>::widen(w[u], acc[u]);
+      }
+    }
+    for (int q = 1; q < N; q++) {
+      const T* src = reinterpret_cast<const T*>(a.send[q]);
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+        if (p < npack) w[u] = ld_stream_v4(src + p * P);
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+        if (p < npack) {
+          float v[8];
+          OsPack<T>::widen(w[u], v);
+#pragma unroll
+          for (int j = 0; j < P; j++) acc[u][j] = __fadd_rn(acc[u][j], v[j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+      if (p < npack) st_v4(out + p * P, OsPack<T>::narrow(acc[u]));
+    }
+  }
+  // ragged end (fewer than one 16-byte pack): tile 0 of each rank
+  if (tile == 0) {
+    for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kOneShotThreads) {
+      float acc = os_scalar<T>(reinterpret_cast<const T*>(a.send[0]) + e);
+      for (int q = 1; q < N; q++) acc = __fadd_rn(acc, os_scalar<T>(reinterpret_cast<const T*>(a.send[q]) + e));
+      os_store_scalar<T>(out + e, acc);
+    }
+  }
+}
+
+cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
+  const int P = a.dtype == kF32 ? 4 : 8;
+  const int64_t npack = a.count / P;
+  const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  static int sm_count[64] = {0};
+  int sms = device < 64 ? sm_count[device] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    if (device < 64) sm_count[device] = sms;
+  }
+  // enough tiles to fill every SM several times over, never more than needed
+  int64_t tiles = div_up(npack, per_tile);
+  const int64_t cap = div_up((int64_t)sms * 8, a.nranks);
+  if (tiles > cap) tiles = cap;
+  if (tiles < 1) tiles = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * a.nranks));
+  cfg.blockDim = dim3(kOneShotThreads);
+  cfg.stream = stream;
+  if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_kernel<float>, a);
+  return cudaLaunchKernelEx(&cfg, oneshot_kernel<uint16_t>, a);
+}
+
+}  // namespace rar

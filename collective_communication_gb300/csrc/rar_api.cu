@@ -1,0 +1,265 @@
+// rar_api.cu -- the C ABI of librar.so (declared in include/rar.h): argument
+// checks, ring setup, workspace sizing and initialisation, launches, status.
+//
+// Pages cited (by title, then section):
+//   [C23] "NCCL 专家课程 23：Device Kernel、Primitives、Step/Credit 与 LL Flag"
+//   [C12] "NCCL 专家课程 12：Ring AllReduce 逐步推导、真实 Ring 与 Channel 并行"
+//         sections "ring index 如何计算", "Graph 如何变成完整 ring"
+//   [OS89] "perf(osar): all-reduce 5커널 → 3커널 (가드·웨이트 프롤로그 융합) - #89"
+//          (review finding: an empty input must not advance any state)
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+
+#include "rar.h"
+#include "rar_launch.h"
+
+namespace rar {
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{0};
+std::atomic<int> g_fault{0};
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+uint64_t spin_timeout_ns() {
+  uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
+  if (t != 0) return t;
+  const char* env = std::getenv("RAR_SPIN_TIMEOUT_NS");
+  if (env != nullptr) {
+    unsigned long long v = std::strtoull(env, nullptr, 10);
+    if (v > 0) return (uint64_t)v;
+  }
+  return kDefaultTimeoutNs;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Ring setup ([C12] "ring index 如何计算"): check that following `next` from
+// rank 0 visits every rank once and comes back ("ring does not loop back"),
+// then ring_index[r] = (place(r) - place(0) + n) % n.
+rar_status setup_ring(int n, const int* ring_order, int* ring_index) {
+  if (ring_order == nullptr) return RAR_ERR_ARG;
+  int place[kMaxRanks], nxt[kMaxRanks];
+  bool seen[kMaxRanks];
+  for (int r = 0; r < n; r++) { place[r] = -1; nxt[r] = -1; seen[r] = false; }
+  for (int i = 0; i < n; i++) {
+    const int r = ring_order[i];
+    if (r < 0 || r >= n || place[r] != -1) return RAR_ERR_RING;
+    place[r] = i;
+    nxt[r] = ring_order[(i + 1) % n];
+  }
+  int cur = 0;
+  for (int i = 0; i < n; i++) {
+    if (cur < 0 || seen[cur]) return RAR_ERR_RING;
+    seen[cur] = true;
+    cur = nxt[cur];
+  }
+  if (cur != 0) return RAR_ERR_RING;
+  for (int r = 0; r < n; r++) ring_index[r] = (place[r] - place[0] + n) % n;
+  return RAR_OK;
+}
+
+bool overlaps(const void* a, const void* b, int64_t bytes) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + (uintptr_t)bytes && y < x + (uintptr_t)bytes;
+}
+
+// Buffers: non-null, 16-byte aligned; a receive buffer may coincide exactly
+// with its own rank's send buffer (in place) and must not overlap anything
+// else. With allow_in_place false it may not touch any send buffer.
+rar_status check_buffers(const void* const* send, void* const* recv, int n, int64_t bytes, bool allow_in_place) {
+  if (send == nullptr || recv == nullptr) return RAR_ERR_ARG;
+  for (int r = 0; r < n; r++) {
+    if (send[r] == nullptr || recv[r] == nullptr) return RAR_ERR_ARG;
+    if (!aligned16(send[r]) || !aligned16(recv[r])) return RAR_ERR_ALIGN;
+  }
+  for (int r = 0; r < n; r++) {
+    for (int q = 0; q < n; q++) {
+      if (q != r && overlaps(recv[r], recv[q], bytes)) return RAR_ERR_ARG;
+      if (overlaps(recv[r], send[q], bytes)) {
+        const bool in_place = allow_in_place && q == r && recv[r] == send[r];
+        if (!in_place) return RAR_ERR_ARG;
+      }
+    }
+  }
+  return RAR_OK;
+}
+
+rar_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return RAR_OK;
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    (void)cudaGetLastError();  // the launch was refused; do not leave it sticky
+    return RAR_ERR_CORESIDENCY;
+  }
+  (void)cudaGetLastError();
+  return RAR_ERR_CUDA;
+}
+
+__global__ void init_header_kernel(char* ws, int nranks, uint64_t mask, int proto, int64_t buff_size) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    WsHeader* h = reinterpret_cast<WsHeader*>(ws);
+    h->status = 0;
+    h->abort = 0;
+    h->nranks = nranks;
+    h->mask = mask;
+    h->proto = proto;
+    h->buff_size = buff_size;
+    h->err_info = 0;
+    h->err_step = 0;
+    h->magic = kMagic;
+  }
+}
+
+}  // namespace
+}  // namespace rar
+
+using namespace rar;
+
+extern "C" {
+
+size_t rar_workspace_bytes(int nranks, uint64_t channelMask, rar_proto proto, size_t buffSize) {
+  Geometry g;
+  if (make_geometry(&g, (int)proto, kF32, nranks, channelMask, 0, (int64_t)buffSize, 4) != 0) return 0;
+  return (size_t)workspace_bytes_for(nranks, g.nchan, g.buff_size);
+}
+
+rar_status rar_workspace_init(void* workspace, size_t workspaceBytes, int nranks, uint64_t channelMask,
+                              rar_proto proto, size_t buffSize, void* stream) {
+  Geometry g;
+  if (make_geometry(&g, (int)proto, kF32, nranks, channelMask, 0, (int64_t)buffSize, 4) != 0) return RAR_ERR_ARG;
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
+  const int64_t need = workspace_bytes_for(nranks, g.nchan, g.buff_size);
+  if ((int64_t)workspaceBytes < need) return RAR_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)need, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  init_header_kernel<<<1, 32, 0, s>>>((char*)workspace, nranks, channelMask, (int)proto, g.buff_size);
+  return from_cuda(cudaGetLastError());
+}
+
+rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                         rar_dtype dtype, rar_redop op, const int* ring_order, uint64_t channelMask,
+                         rar_proto proto, size_t buffSize, int chunkSteps, void* workspace, size_t workspaceBytes,
+                         void* stream) {
+  if (op != RAR_SUM) return RAR_ERR_ARG;
+  if (count > (size_t)INT64_MAX / 4) return RAR_ERR_ARG;
+  Geometry g;
+  if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
+                    chunkSteps) != 0)
+    return RAR_ERR_ARG;
+  RingArgs a;
+  std::memset(&a, 0, sizeof a);
+  rar_status st = setup_ring(nranks, ring_order, a.ring_index);
+  if (st != RAR_OK) return st;
+  st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * g.elem_bytes, true);
+  if (st != RAR_OK) return st;
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
+  if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, g.nchan, g.buff_size)) return RAR_ERR_WORKSPACE;
+  // An empty call enqueues nothing and advances no step counter ([OS89],
+  // review of the empty-input case).
+  if (count == 0) return RAR_OK;
+  for (int r = 0; r < nranks; r++) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  a.geo = g;
+  a.mask = channelMask;
+  a.ws = (char*)workspace;
+  a.conn_offset = kHeaderBytes;
+  a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
+  a.timeout_ns = spin_timeout_ns();
+  a.fault = g_fault.load(std::memory_order_relaxed);
+  const int grid = nranks * g.nchan;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = (g.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr) : launch_ring_line(a, grid, s, nullptr);
+  return from_cuda(e);
+}
+
+rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                       rar_dtype dtype, rar_redop op, void* stream) {
+  if (op != RAR_SUM) return RAR_ERR_ARG;
+  if (nranks < 1 || nranks > kMaxRanks) return RAR_ERR_ARG;
+  if (dtype != RAR_F32 && dtype != RAR_BF16) return RAR_ERR_ARG;
+  if (count > (size_t)INT64_MAX / 4) return RAR_ERR_ARG;
+  const int64_t esz = dtype == RAR_F32 ? 4 : 2;
+  rar_status st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * esz, false);
+  if (st != RAR_OK) return st;
+  if (count == 0) return RAR_OK;
+  OneShotArgs a;
+  std::memset(&a, 0, sizeof a);
+  for (int r = 0; r < nranks; r++) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  a.nranks = nranks;
+  a.dtype = (int)dtype;
+  a.count = (int64_t)count;
+  return from_cuda(launch_oneshot(a, (cudaStream_t)stream));
+}
+
+rar_status rar_get_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e);
+  uint32_t status = 0;
+  e = cudaMemcpy(&status, (char*)workspace + offsetof(WsHeader, status), sizeof status, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (status != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy((char*)workspace + offsetof(WsHeader, status), &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return (rar_status)status;
+}
+
+const char* rar_strerror(rar_status status) {
+  switch (status) {
+    case RAR_OK: return "success";
+    case RAR_ERR_ARG: return "invalid argument";
+    case RAR_ERR_RING: return "ring_order is not one ring over all ranks (ring does not loop back)";
+    case RAR_ERR_ALIGN: return "buffer or workspace not aligned (16 bytes; workspace 256 bytes)";
+    case RAR_ERR_WORKSPACE: return "workspace too small or not initialised for this configuration";
+    case RAR_ERR_CORESIDENCY: return "the (rank, channel) blocks cannot all be resident on the GPU at once";
+    case RAR_ERR_CUDA: return "a CUDA runtime call failed";
+    case RAR_ERR_TIMEOUT: return "a device wait ran past its time limit; the workspace is aborted";
+    case RAR_ERR_ABORT: return "the workspace was aborted by an earlier failure; re-initialise it";
+  }
+  return "unknown status";
+}
+
+void rar_set_spin_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns, std::memory_order_relaxed); }
+
+void rar_debug_set_fault(int fault) { g_fault.store(fault, std::memory_order_relaxed); }
+
+rar_status rar_describe_geometry(int nranks, size_t count, rar_dtype dtype, uint64_t channelMask, rar_proto proto,
+                                 size_t buffSize, int chunkSteps, int64_t* out) {
+  if (out == nullptr) return RAR_ERR_ARG;
+  Geometry g;
+  if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
+                    chunkSteps) != 0)
+    return RAR_ERR_ARG;
+  const int C = g.nchan;
+  out[0] = g.step_bytes;
+  out[1] = g.chunk_elems;
+  out[2] = g.sps;
+  out[3] = g.spc;
+  out[4] = C;
+  out[5] = g.per_channel;
+  int n = 0;
+  for (int b = 0; b < kMaxChannels; b++)
+    if ((channelMask >> b) & 1ull) out[6 + n++] = b;
+  for (int c = 0; c < C; c++) {
+    int64_t go, cc;
+    channel_range(g, c, &go, &cc);
+    out[6 + C + 2 * c] = go;
+    out[6 + C + 2 * c + 1] = cc;
+    out[6 + 3 * C + c] = div_up(cc, loop_count(g));
+  }
+  return RAR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// rar_device.cuh -- workspace layout, kernel arguments and device helpers
+// (inline PTX for loads/stores with explicit scope and caching, fences,
+// mbarriers, bounded waits) of librar.so. sm_103a only.
+//
+// Pages cited (by title, then section):
+//   [C23] "NCCL 专家课程 23：Device Kernel、Primitives、Step/Credit 与 LL Flag"
+//   [NOTES] "NCCL" notes (cishoon.github.io), section "Memory Model（acquire / release
+//           真正在做什么）"
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "rar_geometry.h"
+
+namespace rar {
+
+// ---------------------------------------------------------------------------
+// Workspace layout (device memory owned by the caller).
+//   [0, 4096)            WsHeader, then a per-block channel-id trace at 2048
+//   [4096, 4096 + R)     one ConnCounters record (256 B) per connection
+//   [4096 + R, ...)      one FIFO of buff_size bytes per connection
+// R = align_up(C * N * 256, 4096). Connection (dense channel n, ring edge e)
+// is number n * N + e; edge e runs from ring index e to ring index e + 1.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMagic = 0x31524152u;  // "RAR1"
+constexpr int64_t kHeaderBytes = 4096;
+constexpr int64_t kTraceOffset = 2048;
+constexpr int64_t kConnBytes = 256;
+
+struct WsHeader {
+  uint32_t magic;
+  uint32_t status;     // first device failure (rar_status), 0 if none
+  uint32_t abort;      // raised by the first block that gives up
+  int32_t nranks;
+  uint64_t mask;
+  int32_t proto;
+  int32_t pad0;
+  int64_t buff_size;   // resolved (never 0)
+  uint64_t err_info;   // where the first failure happened: block << 32 | role << 24 | slice
+  uint64_t err_step;   // the step it waited for
+};
+
+// head: steps the receiver has released; tail: steps the sender has published
+// (Simple), or the sender's step count at the end of a call (LL, LL128). Each
+// on its own 128-byte line so that the two sides' polls do not share a line.
+struct ConnCounters {
+  uint64_t head;
+  uint64_t pad0[15];
+  uint64_t tail;
+  uint64_t pad1[15];
+};
+
+inline int64_t conn_region_bytes(int nranks, int nchan) {
+  return align_up((int64_t)nranks * nchan * kConnBytes, 4096);
+}
+inline int64_t workspace_bytes_for(int nranks, int nchan, int64_t buff_size) {
+  return kHeaderBytes + conn_region_bytes(nranks, nchan) + (int64_t)nranks * nchan * buff_size;
+}
+
+// Status codes written by kernels (mirror rar_status).
+constexpr uint32_t kErrWorkspace = 4;
+constexpr uint32_t kErrTimeout = 7;
+constexpr uint32_t kErrAbort = 8;
+
+// Fault injection for tests (a wait that nothing satisfies; the wait runs out
+// of time and the launch ends with RAR_ERR_TIMEOUT).
+constexpr int kFaultNone = 0;
+constexpr int kFaultDropHead = 1;   // receivers never publish their head
+
+struct RingArgs {
+  const void* send[kMaxRanks];
+  void* recv[kMaxRanks];
+  int ring_index[kMaxRanks];  // ring index of user rank r
+  Geometry geo;
+  uint64_t mask;
+  char* ws;                    // workspace base
+  int64_t conn_offset;         // byte offset of the ConnCounters array
+  int64_t fifo_offset;         // byte offset of the FIFO array
+  uint64_t timeout_ns;
+  int fault;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers. Scope .gpu: every party (the N ranks' blocks) is an SM of the
+// same GPU, so the system scope the pages need for peers across NVLink, the
+// CPU proxy or a NIC is not required here ([NOTES] Memory Model).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// FIFO payload reads: cached in L2 only, so a slot reused NCCL_STEPS steps
+// later is never served from a stale L1 line.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_cg_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_cg_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// User input reads: streamed, not kept in L1. (Not the non-coherent path:
+// an in-place call writes the same buffer later in the kernel.)
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+// Line polls and line stores of LL / LL128: one 16-byte access each, so a
+// line's data and its flag(s) travel together ([C23] "LL：Data 与 Flag 同 Line").
+__device__ __forceinline__ uint4 ld_volatile_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_volatile_v4(void* p, uint4 v) {
+  asm volatile("st.volatile.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// mbarrier in shared memory (one phase bit per completed round).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Failure reporting and bounded waits ([C23] checkAbort in the wait loops).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ WsHeader* header_of(const RingArgs& a) { return (WsHeader*)a.ws; }
+
+__device__ __forceinline__ void report_failure(WsHeader* h, uint32_t code, uint64_t info, uint64_t step) {
+  if (atomicCAS(&h->status, 0u, code) == 0u) {
+    h->err_info = info;
+    h->err_step = step;
+  }
+  atomicExch(&h->abort, 1u);
+}
+
+// Iteration backstop, in case the timer misbehaves: far above what any
+// legitimate wait needs, still a finite wait.
+constexpr uint32_t kMaxSpinChecks = 1u << 24;
+
+// State of one bounded wait. poll() returns true when the wait must give up
+// (time limit passed, or another block raised the abort flag).
+struct Spin {
+  uint64_t t0;
+  uint32_t iters;
+  uint32_t checks;
+  __device__ __forceinline__ Spin() : t0(0), iters(0), checks(0) {}
+  __device__ __forceinline__ bool poll(const RingArgs& a, uint64_t info, uint64_t step) {
+    if ((++iters & 63u) != 0u) return false;
+    WsHeader* h = header_of(a);
+    if (ld_relaxed_u32(&h->abort) != 0u) return true;
+    uint64_t now = global_timer_ns();
+    if (t0 == 0) t0 = now;
+    if (now - t0 > a.timeout_ns || ++checks > kMaxSpinChecks) {
+      report_failure(h, kErrTimeout, info, step);
+      return true;
+    }
+    return false;
+  }
+};
+
+// Bounded wait on an mbarrier phase. Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait(const RingArgs& a, uint64_t* bar, uint32_t parity, uint64_t info) {
+  Spin sp;
+  while (!mbar_try_wait(bar, parity)) {
+    if (sp.poll(a, info, parity)) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ ConnCounters* conn_at(const RingArgs& a, int dense_channel, int edge) {
+  return (ConnCounters*)(a.ws + a.conn_offset) + ((int64_t)dense_channel * a.geo.nranks + edge);
+}
+__device__ __forceinline__ char* fifo_at(const RingArgs& a, int dense_channel, int edge) {
+  return a.ws + a.fifo_offset + ((int64_t)dense_channel * a.geo.nranks + edge) * a.geo.buff_size;
+}
+
+// Block -> (rank, dense channel, channel id). Block b serves rank b / C and
+// the (b % C)-th set bit of the mask; each thread below 64 tests one bit the
+// way the page's kernel entry does: n = popcount(mask & ((1 << id) - 1))
+// ([C23] "Kernel 如何把 Block 映射到 Channel").
+__device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* dense, int* sh_chan_id) {
+  int C = a.geo.nchan;
+  *rank = blockIdx.x / C;
+  *dense = blockIdx.x % C;
+  int tid = threadIdx.x;
+  if (tid < kMaxChannels && ((a.mask >> tid) & 1ull)) {
+    uint64_t below = tid == 0 ? 0ull : (a.mask & ((1ull << tid) - 1ull));
+    if (__popcll(below) == *dense) *sh_chan_id = tid;
+  }
+}
+
+// Entry check shared by the ring kernels (thread 0): the workspace must be
+// initialised for this configuration and not aborted. Returns true to run.
+__device__ __forceinline__ bool entry_check(const RingArgs& a) {
+  WsHeader* h = header_of(a);
+  if (h->magic != kMagic || h->nranks != a.geo.nranks || h->mask != a.mask || h->proto != a.geo.proto ||
+      h->buff_size != a.geo.buff_size) {
+    report_failure(h, kErrWorkspace, (uint64_t)blockIdx.x << 32, 0);
+    return false;
+  }
+  if (ld_relaxed_u32(&h->abort) != 0u) {
+    atomicCAS(&h->status, 0u, kErrAbort);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint64_t round_up_steps(uint64_t v) {
+  return (v + kSteps - 1) / kSteps * kSteps;
+}
+
+// bf16 helpers: widening is exact (a bf16 is the upper half of a binary32);
+// narrowing is round-to-nearest-even by the hardware conversion.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace rar

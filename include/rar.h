@@ -1,0 +1,203 @@
+/*
+ * rar.h -- C ABI of the ring AllReduce library (librar.so) for one GB300.
+ *
+ * N "virtual ranks" live in one GPU: every rank's send buffer, receive buffer
+ * and connector FIFOs are ordinary device memory of that GPU, and one kernel
+ * launch runs all ranks at once (one thread block per (rank, channel)).
+ *
+ * Pages the operations follow (cited by title and section):
+ *   [C23] "NCCL 专家课程 23：Device Kernel、Primitives、Step/Credit 与 LL Flag"
+ *   [C12] "NCCL 专家课程 12：Ring AllReduce 逐步推导、真实 Ring 与 Channel 并行"
+ *   [NOTES] "NCCL" notes (cishoon.github.io), sections "2 CUDA stream",
+ *           "5 Symmetric Memory"
+ *   [OS89] "perf(osar): all-reduce 5커널 → 3커널 (가드·웨이트 프롤로그 융합) - #89"
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *buf*, workspace and the arrays they point to are DEVICE
+ *    memory of the current CUDA device, owned by the caller; the library
+ *    allocates nothing and keeps no pointer after a call returns.
+ *  - Arrays of pointers (sendbufs, recvbufs) and ring_order are HOST arrays of
+ *    nranks entries, read during the call only.
+ *  - `stream` is a cudaStream_t (passed as void*). Work is enqueued on it and
+ *    the call returns without waiting ([NOTES] "2 CUDA stream"). NULL means
+ *    the legacy default stream, which serialises with other streams.
+ *  - Argument errors are reported synchronously by the return value and
+ *    enqueue nothing. Failures found on the device (a wait that ran out of
+ *    time, a workspace not initialised for this call) are written to a status
+ *    word in the workspace and read with rar_get_status().
+ *  - Thread safety: calls that share a workspace must be ordered on one
+ *    stream; calls on different workspaces are independent.
+ */
+#ifndef RAR_H
+#define RAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RAR_API __attribute__((visibility("default")))
+#else
+#define RAR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rar_status {
+  RAR_OK = 0,
+  RAR_ERR_ARG = 1,         /* a bad argument: sizes, enums, chunkSteps, buffSize, aliasing */
+  RAR_ERR_RING = 2,        /* ring_order is not one ring over all ranks ([C12] "Graph 如何变成完整 ring") */
+  RAR_ERR_ALIGN = 3,       /* a buffer or the workspace is not 16-byte aligned */
+  RAR_ERR_WORKSPACE = 4,   /* workspace too small, or not initialised for this configuration */
+  RAR_ERR_CORESIDENCY = 5, /* the (rank, channel) blocks cannot all be resident at once */
+  RAR_ERR_CUDA = 6,        /* a CUDA runtime call failed */
+  RAR_ERR_TIMEOUT = 7,     /* device: a wait ran past its time limit; the kernel gave up */
+  RAR_ERR_ABORT = 8        /* device: the workspace was aborted by an earlier failure */
+} rar_status;
+
+typedef enum rar_dtype { RAR_F32 = 0, RAR_BF16 = 1 } rar_dtype;
+typedef enum rar_redop { RAR_SUM = 0 } rar_redop;
+typedef enum rar_proto { RAR_LL = 0, RAR_LL128 = 1, RAR_SIMPLE = 2 } rar_proto;
+
+#define RAR_NCCL_STEPS 8    /* slots of every connector FIFO ([C23] "Simple 的 Credit 与 Step") */
+#define RAR_MAX_RANKS 32
+#define RAR_MAX_CHANNELS 64 /* bits of channelMask */
+
+/*
+ * Bytes of device workspace a ring AllReduce with these parameters needs.
+ * buffSize 0 selects the protocol's default (Simple 4 MiB, LL 512 KiB,
+ * LL128 4915200 bytes). Layout: a 4 KiB header (status word, abort flag, the
+ * configuration it was initialised for, a per-block trace), then a 256-byte
+ * head/tail record per connection, then one FIFO of buffSize bytes per
+ * connection; a connection is one (channel, ring edge) pair, so there are
+ * nranks * popcount(channelMask) of each. Returns 0 for invalid arguments.
+ */
+RAR_API size_t rar_workspace_bytes(int nranks, uint64_t channelMask, rar_proto proto, size_t buffSize);
+
+/*
+ * Prepare a workspace for ring AllReduce calls with this (nranks,
+ * channelMask, proto, buffSize): zeroes it (FIFO lines, step counters,
+ * status, abort flag) and records the configuration in its header.
+ * Enqueued on `stream`. Must be called once before the first rar_allreduce
+ * on a workspace, again after switching any of these four parameters, and
+ * again after the device reported RAR_ERR_TIMEOUT or RAR_ERR_ABORT.
+ * workspace must be 256-byte aligned.
+ */
+RAR_API rar_status rar_workspace_init(void* workspace, size_t workspaceBytes, int nranks,
+                              uint64_t channelMask, rar_proto proto, size_t buffSize,
+                              void* stream);
+
+/*
+ * Ring AllReduce (sum) over nranks virtual ranks: afterwards every
+ * recvbufs[r][i] holds the sum over all ranks q of sendbufs[q][i].
+ *
+ * Method ([C12] "runRing 的数据切分" .. "源码步骤五", [C23] "Ring AllReduce 到
+ * Primitive"): the channels of channelMask split the buffer into contiguous
+ * ranges; each channel moves its range in loops of nranks chunks; in each loop
+ * the rank at ring index i runs 2*nranks-1 rows -- send, nranks-2 x
+ * recvReduceSend, recvReduceCopySend, nranks-2 x recvCopySend, recv -- on
+ * chunk (i - s - 1) mod nranks at row s, exchanging data only with its ring
+ * neighbours through per-connection FIFOs of RAR_NCCL_STEPS slots under the
+ * chosen protocol ([C23] "Simple 的 Credit 与 Step", "LL：Data 与 Flag 同 Line",
+ * "LL128：15/16 Payload").
+ *
+ * Result: the partial sum of chunk c starts with the input of ring index
+ * c+1 and each following rank adds its input, the owner (index c) last; for
+ * bf16 the partial sums travel as binary32 and are rounded once to bf16 by
+ * the owner. The value is fully determined by (inputs, ring_order,
+ * channelMask, proto, buffSize, chunkSteps) and is identical on every rank.
+ *
+ * sendbufs, recvbufs: host arrays of nranks device pointers, 16-byte aligned,
+ *   count elements each. recvbufs[r] == sendbufs[r] (in place) is allowed;
+ *   any other overlap between buffers is RAR_ERR_ARG.
+ * count: elements per rank; 0 enqueues nothing and returns RAR_OK.
+ * dtype: RAR_F32 or RAR_BF16. op: RAR_SUM.
+ * ring_order: host array of nranks user ranks in ring order (next direction);
+ *   must be a permutation of 0..nranks-1, else RAR_ERR_RING.
+ * channelMask: non-zero; block n of each rank serves the n-th set bit
+ *   ([C23] "Kernel 如何把 Block 映射到 Channel").
+ * proto: RAR_SIMPLE, RAR_LL or RAR_LL128.
+ * buffSize: FIFO bytes per connection (0 = default); a multiple of 4096.
+ *   Must match the workspace.
+ * chunkSteps: FIFO steps per Simple chunk: 1, 2 or 4 (8 would fill the whole
+ *   credit window with one chunk and deadlock the ring); LL and LL128 use one
+ *   step per chunk but still require 1, 2 or 4.
+ * workspace: initialised by rar_workspace_init for the same nranks,
+ *   channelMask, proto and buffSize; workspaceBytes >= rar_workspace_bytes().
+ *   Its step counters carry over from call to call, so FIFO contents never
+ *   need clearing between calls.
+ * Errors: RAR_ERR_ARG, RAR_ERR_RING, RAR_ERR_ALIGN, RAR_ERR_WORKSPACE,
+ *   RAR_ERR_CORESIDENCY, RAR_ERR_CUDA (synchronous); RAR_ERR_TIMEOUT,
+ *   RAR_ERR_WORKSPACE, RAR_ERR_ABORT later through rar_get_status().
+ */
+RAR_API rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                         size_t count, rar_dtype dtype, rar_redop op, const int* ring_order,
+                         uint64_t channelMask, rar_proto proto, size_t buffSize, int chunkSteps,
+                         void* workspace, size_t workspaceBytes, void* stream);
+
+/*
+ * One-shot AllReduce (sum) over nranks virtual ranks ([OS89], the single
+ * kernel form; [NOTES] "5 Symmetric Memory": a rank reads its peers' buffers
+ * by pointer): every rank reads all peers' inputs and reduces them itself,
+ * in binary32, in user-rank order 0..nranks-1, rounding once for bf16:
+ *   recvbufs[r][i] = T(((x_0[i] + x_1[i]) + x_2[i]) + ... + x_{n-1}[i]).
+ * sendbufs, recvbufs: host arrays of nranks device pointers, 16-byte aligned,
+ *   count elements each; a receive buffer may not overlap any send buffer
+ *   (the ranks read each other's inputs while writing their outputs) nor
+ *   another receive buffer, else RAR_ERR_ARG.
+ * dtype: RAR_BF16 or RAR_F32; op: RAR_SUM; count 0 returns RAR_OK.
+ * Needs no workspace. Errors: RAR_ERR_ARG, RAR_ERR_ALIGN, RAR_ERR_CUDA.
+ */
+RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                       size_t count, rar_dtype dtype, rar_redop op, void* stream);
+
+/*
+ * Wait for `stream`, then return the device status word of `workspace`
+ * (RAR_OK if no kernel reported a failure) and clear it. After
+ * RAR_ERR_TIMEOUT the workspace stays aborted (later calls report
+ * RAR_ERR_ABORT) until rar_workspace_init.
+ */
+RAR_API rar_status rar_get_status(void* workspace, void* stream);
+
+/* Static text for a status code. */
+RAR_API const char* rar_strerror(rar_status status);
+
+/*
+ * Time limit, in nanoseconds, of every wait inside the kernels (a wait for
+ * data, for a credit, or for another role of the same block). When it runs
+ * out the block records RAR_ERR_TIMEOUT, raises the workspace's abort flag,
+ * and every block leaves its loops, so the launch always completes. Applies
+ * to launches enqueued after the call. Default 2 s; 0 restores the default.
+ */
+RAR_API void rar_set_spin_timeout_ns(uint64_t ns);
+
+/*
+ * Test hook for failure detection: fault 0 = none (default); 1 = every
+ * receiver skips publishing its head, so each sender runs out of credit
+ * after RAR_NCCL_STEPS steps and waits until the time limit. No GPU fault
+ * happens: the waits end, every block leaves, the launch completes, and
+ * rar_get_status() reports RAR_ERR_TIMEOUT. Applies to launches enqueued
+ * after the call.
+ */
+RAR_API void rar_debug_set_fault(int fault);
+
+/*
+ * The geometry a ring AllReduce call would use, computed on the host with
+ * no device work (the "TRACE" view of [C23] "Kernel 如何把 Block 映射到
+ * Channel" and [C12] "runRing 的数据切分"). out receives, in order:
+ *   out[0] step bytes, out[1] full-chunk elements, out[2] steps per slice,
+ *   out[3] slices per chunk, out[4] C = popcount(channelMask), out[5]
+ *   elements per channel, then C channel ids (dense order), then for each
+ *   dense channel its (gridOffset, channelCount), then for each dense
+ *   channel its number of loops.
+ * out must hold 6 + 4*C entries. Returns the status of argument checks.
+ */
+RAR_API rar_status rar_describe_geometry(int nranks, size_t count, rar_dtype dtype, uint64_t channelMask,
+                                 rar_proto proto, size_t buffSize, int chunkSteps, int64_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RAR_H */

@@ -278,7 +278,8 @@ static int geom_init(geom_t* g, int proto, int dtype, int nranks, uint64_t mask,
     /* one step per chunk; each 16-byte line carries 8 payload bytes */
     g->chunk_elems = g->step_bytes / 2 / 4;
   } else if (proto == ORC_LL128) {
-    if (buffSize % 1024 != 0) return ORC_EARG;
+    /* Reading: whole groups of 4 lines per step (a multiple of 4096 bytes). */
+    if (buffSize % 4096 != 0) return ORC_EARG;
     g->step_bytes = buffSize / NSTEPS;
     g->sps = 1;
     g->spc = 1;
@@ -319,10 +320,12 @@ static size_t chunk_nelem(size_t chunkCount, size_t remCount, int c) {
 
 /* Slice size of a chunk of nelem elements ([C23] "Slice Size"): the larger of
  * an even split over SlicePerChunk slices in units of 16 elements and 1/32 of
- * the FIFO capacity of one slice. LL and LL128 use one slice per chunk. */
+ * the FIFO capacity of one slice, aligned to 16 elements (the page's text;
+ * the 1/32 floor is not always a multiple of 16 for the buffer sizes allowed
+ * here). LL and LL128 use one slice per chunk. */
 static size_t slice_size(const geom_t* g, size_t nelem) {
   if (g->proto != ORC_SIMPLE) return nelem;
-  return max_sz(div_up(nelem, 16 * (size_t)g->spc) * 16, g->step_elems * (size_t)g->sps / 32);
+  return align_up(max_sz(div_up(nelem, 16 * (size_t)g->spc) * 16, g->step_elems * (size_t)g->sps / 32), 16);
 }
 
 /*

@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/rar.h declares, rejects bad arguments before touching the device, and
+computes the same geometry as the oracle (two independent implementations)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from collective_communication_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from collective_communication_gb300 import build
+    build.build()
+    return B.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "rar.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rar_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_strerror_covers_every_status(lib):
+    for s in B.Status:
+        assert B.strerror(s)
+
+
+FAKE = 1 << 40  # never dereferenced: every call below fails its checks first
+
+
+def call(n=4, count=1024, dtype=B.Dtype.F32, op=0, ring=None, mask=1, proto=B.Proto.SIMPLE, bs=65536, cs=4,
+         send=None, recv=None, ws=FAKE, wsb=1 << 30):
+    ring = list(range(n)) if ring is None else ring
+    send = [FAKE + (i << 28) for i in range(n)] if send is None else send
+    recv = [FAKE + (1 << 35) + (i << 28) for i in range(n)] if recv is None else recv
+    L = B.load_library()
+    sp = (ctypes.c_void_p * len(send))(*send)
+    rp = (ctypes.c_void_p * len(recv))(*recv)
+    rg = (ctypes.c_int * len(ring))(*ring)
+    return L.rar_allreduce(sp, rp, n, count, int(dtype), op, rg, mask, int(proto), bs, cs, ws, wsb, None)
+
+
+def test_argument_errors(lib):
+    S = B.Status
+    assert call(n=1, ring=[0]) == S.ERR_ARG
+    assert call(n=33, ring=list(range(33))) == S.ERR_ARG
+    assert call(op=1) == S.ERR_ARG
+    assert call(dtype=7) == S.ERR_ARG
+    assert call(proto=9) == S.ERR_ARG
+    assert call(mask=0) == S.ERR_ARG
+    assert call(cs=8) == S.ERR_ARG  # one chunk would fill the credit window: deadlock
+    assert call(cs=3) == S.ERR_ARG
+    assert call(bs=5000) == S.ERR_ARG
+    assert call(proto=B.Proto.LL128, bs=1000) == S.ERR_ARG
+    assert call(ring=[0, 1, 1, 2]) == S.ERR_RING
+    assert call(ring=[0, 1, 2, 4]) == S.ERR_RING
+    assert call(send=[FAKE + 4] + [FAKE + (i << 28) for i in range(1, 4)]) == S.ERR_ALIGN
+    # a receive buffer overlapping another rank's send buffer
+    assert call(recv=[FAKE + (1 << 28)] + [FAKE + (1 << 35) + (i << 28) for i in range(1, 4)]) == S.ERR_ARG
+    # in place is allowed (fails later on the workspace size only)
+    same = [FAKE + (i << 28) for i in range(4)]
+    assert call(send=same, recv=same, wsb=16) == S.ERR_WORKSPACE
+    assert call(ws=0) == S.ERR_WORKSPACE
+    assert call(ws=FAKE + 16) == S.ERR_ALIGN
+    assert call(wsb=16) == S.ERR_WORKSPACE
+    # count 0: nothing is enqueued and nothing fails
+    assert call(count=0) == S.OK
+
+
+def test_oneshot_argument_errors(lib):
+    L = B.load_library()
+    S = B.Status
+    n = 4
+    send = (ctypes.c_void_p * n)(*[FAKE + (i << 28) for i in range(n)])
+    recv = (ctypes.c_void_p * n)(*[FAKE + (1 << 35) + (i << 28) for i in range(n)])
+    assert L.rar_oneshot(send, recv, n, 100, 1, 1, None) == S.ERR_ARG  # op
+    assert L.rar_oneshot(send, recv, n, 100, 5, 0, None) == S.ERR_ARG  # dtype
+    assert L.rar_oneshot(send, recv, 0, 100, 1, 0, None) == S.ERR_ARG
+    assert L.rar_oneshot(send, send, n, 100, 1, 0, None) == S.ERR_ARG  # in place is a race here
+    assert L.rar_oneshot(send, recv, n, 0, 1, 0, None) == S.OK
+
+
+def test_workspace_bytes_formula(lib):
+    for n, mask, proto, bs in [(4, 1, B.Proto.SIMPLE, 65536), (8, 0xFFF, B.Proto.SIMPLE, 1 << 20),
+                               (8, 0b101101011011, B.Proto.LL128, 0), (2, 3, B.Proto.LL, 0)]:
+        c = bin(mask).count("1")
+        bs_eff = bs or oracle.default_buffsize(int(proto))
+        conn = -(-(n * c * 256) // 4096) * 4096
+        assert B.workspace_bytes(n, mask, proto, bs) == 4096 + conn + n * c * bs_eff
+    assert B.workspace_bytes(1, 1, B.Proto.SIMPLE, 0) == 0
+
+
+def _oracle_proto(p):
+    return {B.Proto.LL: oracle.LL, B.Proto.LL128: oracle.LL128, B.Proto.SIMPLE: oracle.SIMPLE}[p]
+
+
+@pytest.mark.parametrize("seed", range(25))
+def test_library_geometry_matches_oracle(lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    n = int(rng.integers(2, 9))
+    proto = B.Proto(int(rng.integers(0, 3)))
+    dtype = B.Dtype(int(rng.integers(0, 2)))
+    mask = int(rng.integers(1, 1 << 63, dtype=np.uint64)) if seed % 3 == 0 else int(rng.integers(1, 1 << 12))
+    count = int(rng.integers(0, 1 << 26))
+    bs = {B.Proto.SIMPLE: 4096 * int(rng.integers(1, 1024)), B.Proto.LL: 4096 * int(rng.integers(1, 256)),
+          B.Proto.LL128: 4096 * int(rng.integers(1, 2000))}[proto]
+    cs = int(rng.choice([1, 2, 4]))
+    got = B.describe_geometry(n, count, dtype, mask, proto, bs, cs)
+    want = oracle.geometry(_oracle_proto(proto), int(dtype), n, mask, count, bs, cs)
+    for k in ("step_bytes", "chunk_elems", "steps_per_slice", "slices_per_chunk", "nchannels", "per_channel",
+              "channel_ids", "channels"):
+        assert got[k] == want[k], k
+    for ch in range(got["nchannels"]):
+        loops = oracle.channel_loops(_oracle_proto(proto), int(dtype), n, mask, count, ch, bs, cs)
+        assert got["loops"][ch] == len(loops)

@@ -1,0 +1,230 @@
+"""GPU parity of the ring AllReduce (all protocols, f32 and bf16) against the
+CPU oracle: bit-exact, element by element, on every rank, with guard bands
+around every receive buffer. Calls go through the C ABI (librar.so)."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+from collective_communication_gb300 import binding as B
+from collective_communication_gb300 import inputs as gen
+from gpu_util import check_guards, device_rows_numpy, guarded_outputs, to_device
+
+pytestmark = pytest.mark.gpu
+
+OPROTO = {"LL": oracle.LL, "LL128": oracle.LL128, "Simple": oracle.SIMPLE}
+ODT = {"f32": oracle.F32, "bf16": oracle.BF16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    B.load_library()
+    B.set_spin_timeout_ns(5_000_000_000)
+    yield
+
+
+def run_ring(case, x=None, in_place=False, workspace=None, calls=1):
+    x = case.inputs() if x is None else x
+    big_in, send = to_device(x, case.dtype)
+    if in_place:
+        big_out, recv = big_in, send
+    else:
+        big_out, recv = guarded_outputs(case.nranks, case.count, case.dtype)
+    ws = workspace or B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    for _ in range(calls):
+        if in_place and calls > 1:
+            raise ValueError
+        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+    st = B.get_status(ws)
+    assert st == B.Status.OK, st
+    if not in_place:
+        check_guards(big_out, case.count, case.dtype)
+    return x, device_rows_numpy(recv, case.dtype), ws
+
+
+def oracle_full(case, x):
+    return oracle.ring_allreduce_closed(list(x), case.ring, case.mask, OPROTO[case.proto], case.buff_size,
+                                        case.chunk_steps)
+
+
+def assert_bit_exact(got, want_rows):
+    for r in range(got.shape[0]):
+        w = want_rows[r]
+        g = got[r]
+        bad = np.nonzero(g.view(np.uint32 if g.dtype == np.float32 else np.uint16) !=
+                         w.view(np.uint32 if w.dtype == np.float32 else np.uint16))[0]
+        assert bad.size == 0, f"rank {r}: {bad.size} mismatches, first at {bad[:8]}"
+
+
+# ---------------------------------------------------------------------------
+# the 4 KiB integer case: every protocol, exact sum
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("proto", ["Simple", "LL", "LL128"])
+def test_small_integer_case_exact(proto):
+    case = gen.small_case()
+    case.proto = proto
+    if proto != "Simple":
+        case.buff_size = 0
+    x, got, _ = run_ring(case)
+    exact = x.astype(np.int64).sum(axis=0).astype(np.float32)
+    for r in range(case.nranks):
+        assert np.array_equal(got[r], exact)
+    assert_bit_exact(got, oracle_full(case, x))
+
+
+# ---------------------------------------------------------------------------
+# 512 KiB per rank, N=4: protocols x channels
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", gen.sweep_512k_cases(), ids=lambda c: c.name)
+def test_sweep_512k(case):
+    x, got, _ = run_ring(case)
+    assert_bit_exact(got, oracle_full(case, x))
+
+
+# ---------------------------------------------------------------------------
+# tiny and ragged cases, several tiles, random rings and masks, both dtypes
+# ---------------------------------------------------------------------------
+def _random_cases():
+    rng = np.random.default_rng(77)
+    out = []
+    for k in range(36):
+        n = int(rng.integers(2, 9))
+        proto = ["LL", "LL128", "Simple"][k % 3]
+        dtype = "f32" if (k // 3) % 2 == 0 else "bf16"
+        mask = int(rng.integers(1, 1 << 8))
+        count = [1, 3, 7, 13, 100, 1000][k % 6] if k < 12 else int(rng.integers(1, 300000))
+        bs = {"Simple": 4096 * int(rng.integers(1, 9)), "LL": 4096 * int(rng.integers(1, 5)),
+              "LL128": 4096 * int(rng.integers(1, 10))}[proto]
+        cs = int(rng.choice([1, 2, 4]))
+        ring = rng.permutation(n).tolist()
+        out.append(gen.RingCase(f"rand{k}_{proto}_{dtype}_n{n}_c{count}", n, ring, mask, proto, count, dtype,
+                                "normal", 1000 + k, bs, cs))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: c.name)
+def test_random_cases(case):
+    x, got, _ = run_ring(case)
+    assert_bit_exact(got, oracle_full(case, x))
+
+
+@pytest.mark.parametrize("proto", ["LL", "LL128", "Simple"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_in_place(proto, dtype):
+    case = gen.RingCase("inplace", 5, [3, 1, 4, 0, 2], 0b1011, proto, 77777, dtype, "normal", 42,
+                        8192 if proto == "Simple" else 0, 4)
+    x = case.inputs()
+    want = oracle_full(case, x)
+    _, got, _ = run_ring(case, x=x, in_place=True)
+    assert_bit_exact(got, want)
+
+
+@pytest.mark.parametrize("proto", ["LL", "LL128", "Simple"])
+def test_many_calls_reuse_workspace(proto):
+    """Step counters carry over between calls: 7 calls with changing data,
+    dtype and ring on one workspace, each bit-exact."""
+    bs = 16384 if proto == "Simple" else 0
+    ws = B.Workspace(4, 0b110, proto, bs)
+    for k in range(7):
+        dtype = "f32" if k % 2 == 0 else "bf16"
+        ring = gen.ring_permutation(4, 500 + k)
+        case = gen.RingCase("reuse", 4, ring, 0b110, proto, 5000 + 997 * k, dtype, "normal", 900 + k, bs,
+                            [4, 2, 1][k % 3])
+        x, got, _ = run_ring(case, workspace=ws)
+        assert_bit_exact(got, oracle_full(case, x))
+
+
+def test_block_to_channel_trace():
+    """The kernel writes, per block, the channel id it mapped itself to; block
+    b serves rank b // C and the (b % C)-th set bit of the mask."""
+    mask = gen.SPARSE_MASK
+    case = gen.RingCase("trace", 3, [0, 2, 1], mask, "Simple", 4096, "f32", "normal", 5, 65536, 4)
+    _, _, ws = run_ring(case)
+    ids = oracle.mask_channels(mask)
+    C = len(ids)
+    trace = ws.tensor[2048:2048 + 3 * C].cpu().numpy()
+    for b in range(3 * C):
+        assert trace[b] == ids[b % C]
+
+
+# ---------------------------------------------------------------------------
+# full size: N=8, 64 MiB per rank (sampled against the oracle; all ranks equal)
+# ---------------------------------------------------------------------------
+def _sample_check(case, x_dev_rows, recv, idx):
+    sampled = [r[idx] for r in x_dev_rows]
+    want, _ = oracle.ring_closed_at(sampled, case.ring, case.mask, OPROTO[case.proto], idx, case.count,
+                                    case.buff_size, case.chunk_steps)
+    for r in range(case.nranks):
+        got = recv[r][idx]
+        assert np.array_equal(got.view(np.uint32 if got.dtype == np.float32 else np.uint16),
+                              want.view(np.uint32 if want.dtype == np.float32 else np.uint16)), f"rank {r}"
+
+
+def _device_inputs(case):
+    """Seeded inputs drawn on the device (too large to draw on the host quickly)."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(case.seed)
+    dt = torch.float32
+    x = torch.randn((case.nranks, case.count), generator=g, device="cuda", dtype=dt)
+    if case.dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    return x
+
+
+def _run_large(case, nsamples=200000):
+    x = _device_inputs(case)
+    send = [x[r] for r in range(case.nranks)]
+    recv_big = torch.empty_like(x)
+    recv = [recv_big[r] for r in range(case.nranks)]
+    ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+    assert B.get_status(ws) == B.Status.OK
+    # every rank holds the same bytes (a property at any size)
+    raw = recv_big.view(torch.int32 if case.dtype == "f32" else torch.int16)
+    for r in range(1, case.nranks):
+        assert bool(torch.equal(raw[r], raw[0])), f"rank {r} differs from rank 0"
+    rng = np.random.default_rng(case.seed)
+    idx = np.unique(np.concatenate([rng.integers(0, case.count, nsamples), np.arange(min(4096, case.count)),
+                                    np.arange(max(0, case.count - 4096), case.count)]))
+    it = torch.from_numpy(idx).cuda()
+    if case.dtype == "f32":
+        xs = [x[r].index_select(0, it).cpu().numpy() for r in range(case.nranks)]
+        rs = [recv_big[r].index_select(0, it).cpu().numpy() for r in range(case.nranks)]
+    else:
+        xs = [x[r].view(torch.int16).index_select(0, it).cpu().numpy().view(np.uint16) for r in range(case.nranks)]
+        rs = [recv_big[r].view(torch.int16).index_select(0, it).cpu().numpy().view(np.uint16)
+              for r in range(case.nranks)]
+    full_idx = np.arange(idx.size)
+    sampled = xs
+    want, _ = oracle.ring_closed_at(sampled, case.ring, case.mask, OPROTO[case.proto], idx, case.count,
+                                    case.buff_size, case.chunk_steps)
+    for r in range(case.nranks):
+        got = rs[r]
+        assert np.array_equal(got.view(np.uint32 if got.dtype == np.float32 else np.uint16),
+                              want.view(np.uint32 if want.dtype == np.float32 else np.uint16)), f"rank {r}"
+    del full_idx
+
+
+@pytest.mark.parametrize("case", gen.large_cases(), ids=lambda c: c.name)
+def test_large_64MiB(case):
+    _run_large(case)
+
+
+def _chunk_elems_of(proto, dtype):
+    return oracle.geometry(OPROTO[proto], ODT[dtype], 8, gen.SPARSE_MASK, 1 << 20)["chunk_elems"]
+
+
+def _sparse_cases():
+    return gen.sparse_sweep_cases(_chunk_elems_of, max_bytes=1 << 30)
+
+
+@pytest.mark.parametrize("case", _sparse_cases(), ids=lambda c: c.name)
+def test_sparse_mask_size_sweep(case):
+    if case.count <= 1 << 20:
+        x, got, _ = run_ring(case)
+        assert_bit_exact(got, oracle_full(case, x))
+    else:
+        _run_large(case, nsamples=50000)

@@ -62,7 +62,7 @@ def test_chunks_partition_the_buffer(seed):
     mask = int(rng.integers(1, 1 << 12))
     count = int(rng.integers(0, 200000))
     bs = {oracle.SIMPLE: 4096 * int(rng.integers(1, 64)), oracle.LL: 4096 * int(rng.integers(1, 16)),
-          oracle.LL128: 1024 * int(rng.integers(8, 64))}[proto]
+          oracle.LL128: 4096 * int(rng.integers(1, 16))}[proto]
     cs = int(rng.choice([1, 2, 4]))
     g, ranges = _chunk_ranges(proto, dtype, n, mask, count, bs, cs)
     E = 16 // (4 if dtype == oracle.F32 else 2)

@@ -86,7 +86,7 @@ def _tiny_cases():
         mask = int(rng.integers(1, 1 << 6))
         count = int(rng.integers(0, 30000)) if k % 5 else int(rng.integers(0, 40))
         bs = {oracle.SIMPLE: 4096 * int(rng.integers(1, 5)), oracle.LL: 4096,
-              oracle.LL128: 1024 * int(rng.integers(8, 20))}[proto]
+              oracle.LL128: 4096 * int(rng.integers(2, 5))}[proto]
         cs = int(rng.choice([1, 2, 4]))
         ring = rng.permutation(n).tolist()
         cases.append((n, proto, dtype, mask, count, bs, cs, ring, int(rng.integers(0, 1 << 30))))
