@@ -1,0 +1,428 @@
+"""Benchmark of the ring AllReduce over N virtual ranks on one GB300.
+
+Headline workload: N=8 virtual ranks, ring order = seeded permutation (seed
+3), f32 sum, 64 MiB per rank of normal(0,1) values, 12 channels (mask 0xFFF),
+Simple protocol with a 1 MiB FIFO buffer and 4 chunk steps. One step = one
+rar_allreduce call (one cooperative launch that runs every rank and channel).
+
+Metric: busBW = (S / t) * 2(N-1)/N in GB/s (1 GB = 1e9 B), S = bytes per rank.
+The JSON line also carries the sweep the metric is quoted "vs size per proto"
+on: every protocol at 64 MiB, LL at 4 KiB, the one-shot variant, each with its
+HBM-roofline fraction.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+With --gpus N > 1 (launched under torchrun) every GPU runs an independent
+replica of the workload (the method keeps all ranks on one GPU: replicas
+only); value = the sum over GPUs of bytes moved / the slowest GPU's time.
+--impl reference times the CPU oracle on the host cores instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring AllReduce busBW"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# headline kernel from one ncu capture of this workload; None until measured
+# for the current kernel (see profiles/).
+TRAFFIC_BYTES_PER_LAUNCH = None
+
+
+def headline_case():
+    from collective_communication_gb300 import inputs as gen
+    ring = gen.ring_permutation(8, 3)
+    return gen.RingCase("n8_f32_64MiB_ch12_simple1M", 8, ring, 0xFFF, gen.SIMPLE, 64 * gen.MIB // 4,
+                        gen.F32, "normal", 3, gen.MIB, 4)
+
+
+def busbw(nbytes_per_rank, nranks, seconds):
+    return nbytes_per_rank / seconds * 2 * (nranks - 1) / nranks / 1e9
+
+
+def wire_factor(proto):
+    return {"Simple": 1.0, "LL128": 16.0 / 15.0, "LL": 2.0}[proto]
+
+
+def algorithmic_bytes(case):
+    """Ideal bytes of one call: every rank reads its input and writes its output
+    once (N * 2S), plus each FIFO byte written once and read once, 2(N-1)/N * S
+    per rank on the wire (LL doubles it, LL128 adds 1/15). bf16 partial sums
+    cross the reduce-scatter half as binary32."""
+    n = case.nranks
+    s = case.count * (4 if case.dtype == "f32" else 2)
+    w = wire_factor(case.proto)
+    if case.dtype == "f32":
+        fifo = n * 2 * (2 * (n - 1) / n * s * w)
+    else:
+        fifo = n * 2 * ((n - 1) / n * 2 * s * w + (n - 1) / n * s * w)
+    return n * 2 * s + fifo
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def device_inputs(case, torch):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(case.seed)
+    x = torch.randn((case.nranks, case.count), generator=g, device="cuda", dtype=torch.float32)
+    if case.dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    return x
+
+
+def time_ring(case, torch, B, steps, warmup):
+    """Device time per call (CUDA events on the launching stream)."""
+    x = device_inputs(case, torch)
+    y = torch.empty_like(x)
+    send = [x[r] for r in range(case.nranks)]
+    recv = [y[r] for r in range(case.nranks)]
+    ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+        b.record(stream)
+    torch.cuda.synchronize()
+    st = B.get_status(ws)
+    if st != B.Status.OK:
+        raise RuntimeError(f"{case.name}: device status {st.name}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    del x, y, ws
+    return ms
+
+
+def sweep(torch, B, steps, warmup, peak):
+    from collective_communication_gb300 import inputs as gen
+    out = {}
+    cases = gen.large_cases()
+    cases.append(gen.RingCase("n8_ll_ch12_64MiB", 8, cases[0].ring, 0xFFF, gen.LL, 64 * gen.MIB // 4,
+                              gen.F32, "normal", 3, 0, 4))
+    for c in cases:
+        ms = time_ring(c, torch, B, steps, warmup)
+        t = statistics.median(ms) / 1e3
+        out[c.name] = {"busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
+                       "us": round(t * 1e6, 1),
+                       "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3),
+                       "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
+    # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel
+    for proto in ("LL", "LL128", "Simple"):
+        c = gen.small_case()
+        c.proto = proto
+        c.buff_size = 64 * gen.KIB if proto == "Simple" else 0
+        ms = time_ring(c, torch, B, max(steps, 20), warmup)
+        out[f"n4_{proto}_ch1_4KiB"] = {"latency_us": round(statistics.median(ms) * 1e3, 2)}
+    # one-shot bf16, N=8, 7168 x {1, 512}
+    for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
+        x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
+                                       case.seed), torch)
+        y = torch.empty_like(x)
+        send = [x[r] for r in range(case.nranks)]
+        recv = [y[r] for r in range(case.nranks)]
+        for _ in range(warmup):
+            B.oneshot(send, recv)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(max(steps, 20))]
+        s = torch.cuda.current_stream()
+        for a, b in ev:
+            a.record(s)
+            B.oneshot(send, recv)
+            b.record(s)
+        torch.cuda.synchronize()
+        t = statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
+        nbytes = case.count * 2
+        out[case.name] = {"us": round(t * 1e6, 2),
+                          "unique_bytes_frac": round(2 * case.nranks * nbytes / t / 1e9 / peak, 3)}
+    return out
+
+
+def e2e_ring(case, torch, B, steps, warmup):
+    """The same call measured end to end from pinned host buffers: every step
+    copies all ranks' inputs host->device, runs the AllReduce and copies every
+    rank's result back."""
+    x = device_inputs(case, torch)
+    host_in = x.cpu().pin_memory()
+    host_out = torch.empty_like(host_in).pin_memory()
+    dx = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    send = [dx[r] for r in range(case.nranks)]
+    recv = [dy[r] for r in range(case.nranks)]
+    ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        dx.copy_(host_in, non_blocking=True)
+        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+        host_out.copy_(dy, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if B.get_status(ws) != B.Status.OK:
+        raise RuntimeError("e2e: device status not OK")
+    t = a.elapsed_time(b) / 1e3 / steps
+    nbytes = case.nranks * case.bytes_per_rank
+    return {"value": round(busbw(case.bytes_per_rank, case.nranks, t), 2), "unit": UNIT,
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": round(t * 1e3, 3)}
+
+
+def cpu_baseline(case, budget_s=10.0):
+    """The CPU oracle's step-by-step simulation of the headline call (full
+    size, same inputs recipe), single-threaded, best of up to 5 runs within
+    about budget_s seconds."""
+    import oracle
+    from collective_communication_gb300 import inputs as gen
+    x = gen.draw("normal", case.nranks, case.count, case.seed, case.dtype)
+    oracle.lib()
+    times = []
+    t_end = time.time() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        oracle.ring_allreduce_sim(list(x), case.ring, case.mask, oracle.SIMPLE, case.buff_size, case.chunk_steps)
+        times.append(time.perf_counter() - t0)
+        if time.time() > t_end or len(times) >= 5:
+            break
+    t = min(times)
+    return {"value": round(busbw(case.bytes_per_rank, case.nranks, t), 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"the whole headline call (8 ranks x 64 MiB f32) through the oracle's step-by-step "
+                      f"simulation, best of {len(times)}, 1 thread; host has {os.cpu_count()} cores",
+            "seconds_per_call": round(t, 3)}
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+    from collective_communication_gb300 import binding as B
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    B.load_library()
+    peak, peak_kind = measured_peak()
+    case = headline_case()
+
+    x = device_inputs(case, torch)
+    y = torch.empty_like(x)
+    send = [x[r] for r in range(case.nranks)]
+    recv = [y[r] for r in range(case.nranks)]
+    ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for a, b in per:
+            a.record(stream)
+            step()
+            b.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = B.get_status(ws)
+    if st != B.Status.OK:
+        raise RuntimeError(f"device status {st.name}")
+    total_ms = start.elapsed_time(end)
+    launch_ms = [a.elapsed_time(b) for a, b in per]
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = busbw(case.bytes_per_rank, case.nranks, ms_per_step / 1e3) * world
+    avg_launch = statistics.mean(launch_ms) / 1e3
+    algo = algorithmic_bytes(case)
+    achieved = algo / avg_launch / 1e9
+    del x, y, ws
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if rank == 0 and not args.no_sweep:
+        extra["sweep"] = sweep(torch, B, max(5, args.steps // 2), args.warmup, peak)
+    e2e = e2e_ring(case, torch, B, max(3, args.steps // 4), args.warmup) if rank == 0 else None
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "ring AllReduce, 8 virtual ranks on one GPU, f32 sum, 64 MiB per rank, "
+                               "ring = seeded permutation (seed 3), 12 channels, Simple, 1 MiB FIFO, 4 chunk steps",
+                   "nranks": case.nranks, "bytes_per_rank": case.bytes_per_rank, "ring_order": case.ring,
+                   "channel_mask": hex(case.mask), "proto": case.proto, "buff_size": case.buff_size,
+                   "chunk_steps": case.chunk_steps,
+                   "l2": "inputs larger than L2 (8 x 64 MiB in, 8 x 64 MiB out per step)",
+                   "parallelism": f"replicas x{world} (no GPU-to-GPU data path)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": TRAFFIC_BYTES_PER_LAUNCH,
+                     "kernel": "ring_simple_kernel<float>", "algorithmic_bytes_per_launch": int(algo),
+                     "peak_kind": f"{peak_kind} copy peak (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "user_bytes_frac": round(case.nranks * 2 * case.bytes_per_rank / avg_launch / 1e9 / peak, 3)},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    line.update(extra)
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is one step-by-step
+    simulation of the whole headline call, single-threaded."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    case = headline_case()
+    from collective_communication_gb300 import inputs as gen
+    x = gen.draw("normal", case.nranks, case.count, case.seed, case.dtype)
+    oracle.lib()
+
+    def one():
+        oracle.ring_allreduce_sim(list(x), case.ring, case.mask, oracle.SIMPLE, case.buff_size, case.chunk_steps)
+
+    for _ in range(min(args.warmup, 1)):
+        one()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    v = busbw(case.bytes_per_rank, case.nranks, t)
+    sample = (f"the whole headline call (8 ranks x 64 MiB f32) through the oracle's step-by-step simulation, "
+              f"1 thread; host has {os.cpu_count()} cores")
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * 1e3, 2), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "ring AllReduce, 8 virtual ranks, f32 sum, 64 MiB per rank, ring = seeded "
+                                   "permutation (seed 3), 12 channels, Simple, 1 MiB FIFO, 4 chunk steps (CPU oracle)"},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

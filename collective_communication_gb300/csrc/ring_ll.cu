@@ -254,8 +254,8 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
   constexpr int UG = 2;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecv = PRIM != kSend;
-  constexpr bool kSendAny = PRIM != kRecv;
+  constexpr bool kHasRecv = PRIM != kSend;
+  constexpr bool kHasSend = PRIM != kRecv;
   constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
   // payload element bytes of this row (both sides)
   constexpr int EB = (PRIM == kSend || PRIM == kRecvReduceSend) ? 4
@@ -273,7 +273,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
     for (int u = 0; u < UG; u++) {
       const int64_t g = g0 + (int64_t)u * NW;
       if (g < ngroups) {
-        if (kRecv) rv[u] = ld_volatile_v4(rslot + g * 512 + 16 * L.lane);
+        if (kHasRecv) rv[u] = ld_volatile_v4(rslot + g * 512 + 16 * L.lane);
         if (kIn) {
           const int64_t e0 = (g * 480 + L.piece_off) / EB;
           const int kv = (int)imax(0, imin(kmax, nelem - e0));
@@ -291,7 +291,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
     for (int u = 0; u < UG; u++) {
       const int64_t g = g0 + (int64_t)u * NW;
       if (g >= ngroups) continue;  // uniform across the warp
-      if (kRecv && !ll128_poll(a, rslot + g * 512 + 16 * L.lane, rflag, L.flag_lane, rv[u], sh_abort, info)) return;
+      if (kHasRecv && !ll128_poll(a, rslot + g * 512 + 16 * L.lane, rflag, L.flag_lane, rv[u], sh_abort, info)) return;
       const int64_t e0 = (g * 480 + L.piece_off) / EB;
       const int kv = (int)imax(0, imin(kmax, nelem - e0));
       uint4 pay;
@@ -314,7 +314,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
         pay = rv[u];  // final values pass through unchanged
       }
       if (kOut && kv > 0) store_out_n<T>(out + e0, kv, kmax, pay);
-      if (kSendAny) {
+      if (kHasSend) {
         if (L.flag_lane) {
           pay.z = (uint32_t)sflag;
           pay.w = (uint32_t)(sflag >> 32);
