@@ -41,6 +41,7 @@ PROTO_BY_NAME = {"LL": Proto.LL, "LL128": Proto.LL128, "Simple": Proto.SIMPLE, "
 EXPORTED = (
     "rar_workspace_bytes", "rar_workspace_init", "rar_allreduce", "rar_oneshot", "rar_get_status",
     "rar_strerror", "rar_set_spin_timeout_ns", "rar_debug_set_fault", "rar_describe_geometry",
+    "rar_allreduce_static",
 )
 
 
@@ -83,6 +84,8 @@ def load_library():
     L.rar_debug_set_fault.restype = None
     L.rar_describe_geometry.argtypes = [I, SZ, I, U64, I, SZ, I, P]
     L.rar_describe_geometry.restype = I
+    L.rar_allreduce_static.argtypes = [P, P, I, SZ, I, I, P, U64, I, SZ, I, P]
+    L.rar_allreduce_static.restype = I
     _lib = L
     return L
 

@@ -153,6 +153,45 @@ RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbuf
                        size_t count, rar_dtype dtype, rar_redop op, void* stream);
 
 /*
+ * Bytes of the device array behind rar_allreduce_static(). Every GPU that
+ * loads this library holds one such array until the process exits.
+ */
+#define RAR_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * rar_allreduce() for callers that cannot allocate device memory -- for
+ * example a plug-in whose host application owns all device memory through
+ * its own allocator, or code on a latency-critical path that may not call
+ * cudaMalloc or cudaFree because those calls can synchronise the whole
+ * device. This entry point allocates nothing: its workspace is a library
+ * array of RAR_STATIC_WORKSPACE_BYTES in device memory (see above). The pages
+ * have no counterpart to it. The caller still passes the send and receive
+ * buffers; every other argument means what it means for rar_allreduce().
+ *
+ * - A call whose workspace (rar_workspace_bytes(nranks, channelMask, proto,
+ *   buffSize)) would exceed RAR_STATIC_WORKSPACE_BYTES is refused with
+ *   RAR_ERR_WORKSPACE and enqueues nothing; invalid arguments give the
+ *   codes of rar_allreduce().
+ * - The first call on a device looks up the array's device address on that
+ *   device (it must be the current device). Make that first call before any
+ *   stream capture begins.
+ * - All calls share the one array, which keeps the last call's contents.
+ *   Each call first clears the part it uses (step counters, status, FIFO
+ *   lines) on `stream`, so no state carries over between calls.
+ * - Calls that overlap on the GPU -- on different streams, or from threads
+ *   whose calls are not ordered on one stream -- race on the array and give
+ *   wrong results. Order them on one stream.
+ * - Device failures are read with rar_get_status() on the array's address,
+ *   which this entry point does not expose; a timed-out call leaves the
+ *   array aborted only until the next call clears it.
+ */
+RAR_API rar_status rar_allreduce_static(const void* const* sendbufs, void* const* recvbufs,
+                                        int nranks, size_t count, rar_dtype dtype, rar_redop op,
+                                        const int* ring_order, uint64_t channelMask,
+                                        rar_proto proto, size_t buffSize, int chunkSteps,
+                                        void* stream);
+
+/*
  * Wait for `stream`, then return the device status word of `workspace`
  * (RAR_OK if no kernel reported a failure) and clear it. After
  * RAR_ERR_TIMEOUT the workspace stays aborted (later calls report
