@@ -39,11 +39,21 @@ FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_BYTES_PER_LAUNCH = None
 
 
-def headline_case():
+def headline_case(args=None):
+    """The headline workload, or a variant of it named on the command line
+    (used to profile smaller cases of the same kernels)."""
     from collective_communication_gb300 import inputs as gen
-    ring = gen.ring_permutation(8, 3)
-    return gen.RingCase("n8_f32_64MiB_ch12_simple1M", 8, ring, 0xFFF, gen.SIMPLE, 64 * gen.MIB // 4,
-                        gen.F32, "normal", 3, gen.MIB, 4)
+    nranks = getattr(args, "nranks", None) or 8
+    ring = gen.ring_permutation(nranks, 3)
+    mib = getattr(args, "mib", None) or 64
+    proto = getattr(args, "proto", None) or gen.SIMPLE
+    buff = getattr(args, "buff_size", None)
+    if buff is None:
+        buff = gen.MIB if proto == gen.SIMPLE else 0
+    chans = getattr(args, "channels", None) or 12
+    name = f"n{nranks}_f32_{mib}MiB_ch{chans}_{proto}{buff // 1024 if buff else 'default'}"
+    return gen.RingCase(name, nranks, ring, (1 << chans) - 1, proto, mib * gen.MIB // 4, gen.F32, "normal", 3,
+                        buff, 4)
 
 
 def busbw(nbytes_per_rank, nranks, seconds):
@@ -181,13 +191,16 @@ def sweep(torch, B, steps, warmup, peak):
                        "us": round(t * 1e6, 1),
                        "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3),
                        "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
-    # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel
+    # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel. Device
+    # latency from a CUDA graph of back-to-back calls (no host enqueue time),
+    # and the stream-launch latency as seen between two events.
     for proto in ("LL", "LL128", "Simple"):
         c = gen.small_case()
         c.proto = proto
         c.buff_size = 64 * gen.KIB if proto == "Simple" else 0
         ms = time_ring(c, torch, B, max(steps, 20), warmup)
-        out[f"n4_{proto}_ch1_4KiB"] = {"latency_us": round(statistics.median(ms) * 1e3, 2)}
+        out[f"n4_{proto}_ch1_4KiB"] = {"stream_latency_us": round(statistics.median(ms) * 1e3, 2),
+                                       "graph_latency_us": graph_latency_ring(c, torch, B)}
     # one-shot bf16, N=8, 7168 x {1, 512}
     for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
         x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
@@ -208,9 +221,53 @@ def sweep(torch, B, steps, warmup, peak):
         torch.cuda.synchronize()
         t = statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
         nbytes = case.count * 2
-        out[case.name] = {"us": round(t * 1e6, 2),
-                          "unique_bytes_frac": round(2 * case.nranks * nbytes / t / 1e9 / peak, 3)}
+        gl = graph_latency(lambda: B.oneshot(send, recv), torch)
+        tg = gl * 1e-6 if gl else t
+        out[case.name] = {"stream_us": round(t * 1e6, 2), "graph_us": gl,
+                          "unique_bytes_frac": round(2 * case.nranks * nbytes / tg / 1e9 / peak, 3)}
     return out
+
+
+def graph_latency(call, torch, reps=50):
+    """Per-call device time of `reps` back-to-back calls captured in one CUDA
+    graph (no host enqueue gaps). None if the capture is refused."""
+    try:
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                call()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                call()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return round(a.elapsed_time(b) * 1e3 / reps, 2)
+    except Exception as e:  # capture not possible: report the reason instead of a number
+        sys.stderr.write(f"graph capture failed: {e}\n")
+        return None
+
+
+def graph_latency_ring(case, torch, B):
+    x = device_inputs(case, torch)
+    y = torch.empty_like(x)
+    send = [x[r] for r in range(case.nranks)]
+    recv = [y[r] for r in range(case.nranks)]
+    ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
+    lat = graph_latency(lambda: B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size,
+                                            case.chunk_steps), torch)
+    if B.get_status(ws) != B.Status.OK:
+        raise RuntimeError("graph replay: device status not OK")
+    return lat
 
 
 def e2e_ring(case, torch, B, steps, warmup):
@@ -286,7 +343,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     B.load_library()
     peak, peak_kind = measured_peak()
-    case = headline_case()
+    case = headline_case(args)
 
     x = device_inputs(case, torch)
     y = torch.empty_like(x)
@@ -336,7 +393,7 @@ def run_gpu(args):
     extra = {}
     if rank == 0 and not args.no_sweep:
         extra["sweep"] = sweep(torch, B, max(5, args.steps // 2), args.warmup, peak)
-    e2e = e2e_ring(case, torch, B, max(3, args.steps // 4), args.warmup) if rank == 0 else None
+    e2e = e2e_ring(case, torch, B, max(3, args.steps // 4), args.warmup) if rank == 0 and not args.no_e2e else None
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -345,16 +402,19 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "ring AllReduce, 8 virtual ranks on one GPU, f32 sum, 64 MiB per rank, "
-                               "ring = seeded permutation (seed 3), 12 channels, Simple, 1 MiB FIFO, 4 chunk steps",
+        "config": {"workload": f"ring AllReduce, {case.nranks} virtual ranks on one GPU, f32 sum, "
+                               f"{case.bytes_per_rank >> 20} MiB per rank, ring = seeded permutation (seed 3), "
+                               f"{bin(case.mask).count('1')} channels, {case.proto}, "
+                               f"{case.buff_size or 'default'} B FIFO, 4 chunk steps",
                    "nranks": case.nranks, "bytes_per_rank": case.bytes_per_rank, "ring_order": case.ring,
                    "channel_mask": hex(case.mask), "proto": case.proto, "buff_size": case.buff_size,
                    "chunk_steps": case.chunk_steps,
-                   "l2": "inputs larger than L2 (8 x 64 MiB in, 8 x 64 MiB out per step)",
+                   "l2": f"inputs larger than L2 ({case.nranks} x {case.bytes_per_rank >> 20} MiB in and out per step)",
                    "parallelism": f"replicas x{world} (no GPU-to-GPU data path)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": TRAFFIC_BYTES_PER_LAUNCH,
-                     "kernel": "ring_simple_kernel<float>", "algorithmic_bytes_per_launch": int(algo),
+                     "kernel": "ring_simple_kernel<float>" if case.proto == "Simple" else "ring_line_kernel<float>",
+                     "algorithmic_bytes_per_launch": int(algo),
                      "peak_kind": f"{peak_kind} copy peak (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
                      "user_bytes_frac": round(case.nranks * 2 * case.bytes_per_rank / avg_launch / 1e9 / peak, 3)},
@@ -415,6 +475,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    # workload variants (profiling): defaults give the headline workload
+    ap.add_argument("--proto", choices=["Simple", "LL", "LL128"])
+    ap.add_argument("--buff-size", type=int)
+    ap.add_argument("--mib", type=int, help="MiB per rank")
+    ap.add_argument("--nranks", type=int)
+    ap.add_argument("--channels", type=int)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -8,19 +8,26 @@
 //   [C12] "NCCL 专家课程 12：Ring AllReduce 逐步推导、真实 Ring 与 Channel 并行"
 //         sections "源码步骤一" .. "源码步骤五"
 //
-// Block organisation (the page's wait / worker / post roles, on Blackwell
-// mbarriers instead of paired named barriers, so the roles run decoupled):
+// Block organisation: the page's wait / worker / post roles, decoupled by
+// shared-memory mbarriers, with the workers' loads moved onto the TMA engine:
 //   warp 0, lane 0  waiter: for slice i, waits until the receive FIFO holds it
 //                   (tail >= step + StepPerSlice) and the send FIFO has room
-//                   (head + NCCL_STEPS >= step + StepPerSlice), then arrives on
-//                   full[i % D];
-//   warps 2..       workers: wait full[i % D], move the slice with 16-byte
-//                   vector loads/stores (reduce in binary32), arrive done[i % D];
-//   warp 1, lane 0  poster: waits done[i % D], then fence.acq_rel.gpu and
-//                   publish tail (payload first, then the tail), publish head,
-//                   arrive empty[i % D] so the waiter may reuse the slot.
-// The waiter may run up to D slices ahead of the poster. Empty slices still
-// wait and post, so both ends of every connection count the same steps.
+//                   (head + NCCL_STEPS >= step + StepPerSlice); arrives ready[i % D].
+//   warp 1, lane 0  loader: after ready[i % D], streams the slice in tiles of
+//                   kTileElems elements: bulk copies (cp.async.bulk) of the user
+//                   input and of the received FIFO bytes into a ring of smem
+//                   stages, completion counted in bytes on full[stage].
+//   warps 3..10     workers: per tile, wait full[stage], reduce from shared
+//                   memory in binary32, store the FIFO output and the user output
+//                   with 16-byte stores, release the stage (empty[stage]); after
+//                   the slice's last tile arrive done[i % D].
+//   warp 2, lane 0  poster: after ready[i % D] and done[i % D], fence.acq_rel.gpu
+//                   then publish the tail (payload first, then the tail) and the
+//                   head; arrive free[i % D] so the waiter may reuse the slot.
+// Up to D slices are in flight between waiter and poster, and up to
+// `nstages` tiles between loader and workers (about 190 KB of loads in flight
+// per SM). Empty slices still wait and post, so both ends of every connection
+// count the same steps.
 #include "rar_device.cuh"
 
 namespace rar {
@@ -127,63 +134,70 @@ __device__ __forceinline__ uint16_t load_final_scalar<uint16_t>(const char* p) {
   return h;
 }
 
-// --- the five primitives on one slice --------------------------------------
-// in/out: user buffers at the slice's first element; rslot/sslot: FIFO bytes
-// of the slice on the receive / send connection.
+// --- one tile of a slice ---------------------------------------------------
+// s_in / s_rcv: the tile's user input and received FIFO bytes in shared
+// memory (the pack-aligned prefix of `covered` elements); g_in / g_out: user
+// buffers at the slice's first element; rslot / sslot: the slice's FIFO bytes
+// on the receive / send connection; e0: the tile's first element in the slice.
 template <typename T, int PRIM>
-__device__ __forceinline__ void move_slice(const T* __restrict__ in, T* __restrict__ out, const char* rslot,
-                                           char* sslot, int64_t nelem, int wt, int nwt) {
+__device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv, const T* __restrict__ g_in,
+                                             T* __restrict__ g_out, const char* rslot, char* sslot, int64_t e0,
+                                             int ne, int covered, int ct, int nct) {
   constexpr int P = ElemTraits<T>::kPack;
-  constexpr int U = ElemTraits<T>::kUnroll;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvFinal = PRIM == kRecvCopySend || PRIM == kRecv;
   constexpr bool kSendPartial = PRIM == kSend || PRIM == kRecvReduceSend;
   constexpr bool kSendFinal = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend;
   constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
-
-  const int64_t npack = nelem / P;
-  for (int64_t p0 = wt; p0 < npack; p0 += (int64_t)nwt * U) {
-    float x[U][P];
-    float part[U][P];
-    uint4 fin[U];
+  constexpr int U = 4;
+  const int npacks = covered / P;
+  for (int j0 = ct; j0 < npacks; j0 += nct * U) {
 #pragma unroll
     for (int u = 0; u < U; u++) {
-      int64_t p = p0 + (int64_t)u * nwt;
-      if (p < npack) {
-        if (kIn) load_input_pack<T>(in + p * P, x[u]);
-        if (kRecvPartial) load_partial_pack<P>(rslot + p * P * 4, part[u]);
-        if (kRecvFinal) fin[u] = ld_cg_v4(rslot + p * 16);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-      int64_t p = p0 + (int64_t)u * nwt;
-      if (p < npack) {
-        if (PRIM == kSend) {
-          store_partial_pack<P>(sslot + p * P * 4, x[u]);
-        } else if (PRIM == kRecvReduceSend) {
-#pragma unroll
-          for (int j = 0; j < P; j++) part[u][j] = __fadd_rn(part[u][j], x[u][j]);
-          store_partial_pack<P>(sslot + p * P * 4, part[u]);
-        } else if (PRIM == kRecvReduceCopySend) {
-#pragma unroll
-          for (int j = 0; j < P; j++) part[u][j] = __fadd_rn(part[u][j], x[u][j]);
-          fin[u] = to_final_pack<T>(part[u]);
+      const int j = j0 + u * nct;
+      if (j < npacks) {
+        const int64_t e = e0 + (int64_t)j * P;
+        float x[P], v[P];
+        uint4 fin;
+        if (kIn) {
+          const uint4 w = *reinterpret_cast<const uint4*>(s_in + j * 16);
+          if constexpr (P == 4) {
+            x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+            x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+          } else {
+            x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+            x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+          }
         }
-        if (kOut) st_v4(out + p * P, fin[u]);
-        if (kSendFinal) st_v4(sslot + p * 16, fin[u]);
-        (void)kSendPartial;
+        if (kRecvPartial) {
+#pragma unroll
+          for (int q = 0; q < P / 4; q++) {
+            const float4 w = *reinterpret_cast<const float4*>(s_rcv + j * P * 4 + 16 * q);
+            v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+          }
+#pragma unroll
+          for (int k = 0; k < P; k++) v[k] = __fadd_rn(v[k], x[k]);
+        } else if (PRIM == kSend) {
+#pragma unroll
+          for (int k = 0; k < P; k++) v[k] = x[k];
+        }
+        if (kRecvFinal) fin = *reinterpret_cast<const uint4*>(s_rcv + j * 16);
+        if (PRIM == kRecvReduceCopySend) fin = to_final_pack<T>(v);
+        if (kSendPartial) store_partial_pack<P>(sslot + e * 4, v);
+        if (kSendFinal) st_v4(sslot + e * (int64_t)sizeof(T), fin);
+        if (kOut) st_v4(g_out + e, fin);
       }
     }
   }
-  // ragged end: fewer than P elements, one per thread
-  for (int64_t e = npack * P + wt; e < nelem; e += nwt) {
+  // the last < P elements of a slice: plain loads straight from global memory
+  for (int k = covered + ct; k < ne; k += nct) {
+    const int64_t e = e0 + k;
     float xv = 0.f, pv = 0.f;
     T fv{};
-    if (kIn) xv = load_input_scalar<T>(in + e);
+    if (kIn) xv = load_input_scalar<T>(g_in + e);
     if (kRecvPartial) pv = __uint_as_float(ld_cg_u32(rslot + e * 4));
-    if (kRecvFinal) fv = load_final_scalar<T>(rslot + e * sizeof(T));
+    if (kRecvFinal) fv = load_final_scalar<T>(rslot + e * (int64_t)sizeof(T));
     if (PRIM == kSend) {
       *reinterpret_cast<float*>(sslot + e * 4) = xv;
     } else if (PRIM == kRecvReduceSend) {
@@ -191,30 +205,52 @@ __device__ __forceinline__ void move_slice(const T* __restrict__ in, T* __restri
     } else if (PRIM == kRecvReduceCopySend) {
       fv = final_scalar<T>(__fadd_rn(pv, xv));
     }
-    if (kOut) out[e] = fv;
-    if (kSendFinal) *reinterpret_cast<T*>(sslot + e * sizeof(T)) = fv;
+    if (kOut) g_out[e] = fv;
+    if (kSendFinal) *reinterpret_cast<T*>(sslot + e * (int64_t)sizeof(T)) = fv;
   }
 }
 
 template <typename T>
-__device__ __forceinline__ void move_slice_any(int prim, const T* in, T* out, const char* rslot, char* sslot,
-                                               int64_t nelem, int wt, int nwt) {
+__device__ __forceinline__ void tile_compute_any(int prim, const char* s_in, const char* s_rcv, const T* g_in,
+                                                 T* g_out, const char* rslot, char* sslot, int64_t e0, int ne,
+                                                 int covered, int ct, int nct) {
   switch (prim) {
-    case kSend: move_slice<T, kSend>(in, out, rslot, sslot, nelem, wt, nwt); break;
-    case kRecvReduceSend: move_slice<T, kRecvReduceSend>(in, out, rslot, sslot, nelem, wt, nwt); break;
-    case kRecvReduceCopySend: move_slice<T, kRecvReduceCopySend>(in, out, rslot, sslot, nelem, wt, nwt); break;
-    case kRecvCopySend: move_slice<T, kRecvCopySend>(in, out, rslot, sslot, nelem, wt, nwt); break;
-    default: move_slice<T, kRecv>(in, out, rslot, sslot, nelem, wt, nwt); break;
+    case kSend: tile_compute<T, kSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct); break;
+    case kRecvReduceSend:
+      tile_compute<T, kRecvReduceSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      break;
+    case kRecvReduceCopySend:
+      tile_compute<T, kRecvReduceCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      break;
+    case kRecvCopySend:
+      tile_compute<T, kRecvCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      break;
+    default: tile_compute<T, kRecv>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct); break;
   }
 }
 
-template <typename T, int NT>
-__global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constant__ RingArgs a) {
-  constexpr int kWorkers = NT - 64;  // warps 2.. are workers
-  __shared__ uint64_t bar_full[kDepth], bar_done[kDepth], bar_empty[kDepth];
+constexpr int kTileElems = 4096;    // elements per bulk-copied tile
+constexpr int kMaxStages = 6;
+constexpr int kComputeWarps = 8;
+constexpr int kComputeThreads = 32 * kComputeWarps;
+constexpr int kSimpleThreads = 32 * 3 + kComputeThreads;  // waiter, loader, poster + workers
+
+template <typename T>
+__host__ __device__ constexpr int stage_bytes() { return kTileElems * ((int)sizeof(T) + 4); }
+
+__device__ __forceinline__ bool recv_is_partial(int prim) { return row_recvs_partial(prim); }
+
+template <typename T>
+__global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __grid_constant__ RingArgs a,
+                                                                        int nstages) {
+  extern __shared__ __align__(128) char smem[];
+  __shared__ uint64_t bar_ready[kDepth], bar_done[kDepth], bar_free[kDepth];
+  __shared__ uint64_t bar_full[kMaxStages], bar_empty[kMaxStages];
   __shared__ volatile int sh_abort;
   __shared__ int sh_chan;
   __shared__ uint64_t sh_base_send, sh_base_recv;
+  constexpr int P = ElemTraits<T>::kPack;
+  constexpr int SB = stage_bytes<T>();
 
   const Geometry& g = a.geo;
   if (threadIdx.x == 0) sh_chan = -1;
@@ -233,9 +269,13 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
   if (threadIdx.x == 0) {
     sh_abort = entry_check(a) ? 0 : 1;
     for (int d = 0; d < kDepth; d++) {
-      mbar_init(&bar_full[d], 1);
-      mbar_init(&bar_done[d], kWorkers);
-      mbar_init(&bar_empty[d], 1);
+      mbar_init(&bar_ready[d], 1);
+      mbar_init(&bar_done[d], kComputeThreads);
+      mbar_init(&bar_free[d], 1);
+    }
+    for (int st = 0; st < kMaxStages; st++) {
+      mbar_init(&bar_full[st], 1);
+      mbar_init(&bar_empty[st], kComputeWarps);
     }
     // This block alone writes the tail of its send edge and the head of its
     // receive edge; both equal the previous call's final step. Slices start
@@ -251,6 +291,9 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
   const uint64_t sps = (uint64_t)g.sps;
   const uint64_t base_send = sh_base_send, base_recv = sh_base_recv;
   const uint64_t info = ((uint64_t)blockIdx.x << 32);
+  const int64_t step_bytes = g.step_bytes;
+  const T* in = reinterpret_cast<const T*>(a.send[rank]);
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
   SliceCursor c;
   cursor_begin(g, dense, ring_idx, c);
 
@@ -260,7 +303,7 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
     uint64_t rstep = base_recv, sstep = base_send, tail_seen = 0, head_seen = 0;
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
-      if (use > 0 && !mbar_wait(a, &bar_empty[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
+      if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
       if (!sh_abort && row_recvs(c.prim)) {
         Spin sp;
         while (tail_seen < rstep + sps) {
@@ -279,18 +322,73 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
           if (sp.poll(a, info | (3u << 24) | i, sstep + sps)) { sh_abort = 1; break; }
         }
       }
-      mbar_arrive(&bar_full[d]);
+      mbar_arrive(&bar_ready[d]);
       if (sh_abort) break;
       if (row_recvs(c.prim)) rstep += sps;
       if (row_sends(c.prim)) sstep += sps;
     }
   } else if (warp == 1) {
     if (lane != 0) return;
+    // ---- loader ----
+    const uint64_t pol = l2_policy_evict_first();
+    uint64_t rstep = base_recv;
+    uint32_t gt = 0;  // tiles issued so far
+    for (uint32_t i = 0; c.valid && !sh_abort; i++, cursor_next(g, c)) {
+      const uint32_t d = i % kDepth, use = i / kDepth;
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) {
+        sh_abort = 1;
+        break;
+      }
+      const int prim = c.prim;
+      const bool has_in = prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend;
+      const bool has_rcv = row_recvs(prim);
+      const int rcv_eb = recv_is_partial(prim) ? 4 : (int)sizeof(T);
+      const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
+      if (has_rcv) fence_proxy_async_global();  // the tail acquired above, before bulk reads of the FIFO
+      const int ntiles = (int)div_up(c.nelem, kTileElems);
+      for (int k = 0; k < ntiles; k++) {
+        const uint32_t st = gt % nstages, su = gt / nstages;
+        if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
+          sh_abort = 1;
+          break;
+        }
+        const int64_t e0 = (int64_t)k * kTileElems;
+        const int ne = (int)imin(kTileElems, c.nelem - e0);
+        const int covered = ne / P * P;
+        const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
+        const uint32_t b_rcv = has_rcv ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
+        char* s_in = smem + (int64_t)st * SB;
+        char* s_rcv = s_in + kTileElems * (int)sizeof(T);
+        mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
+        if (b_in) tma_load_1d(s_in, in + c.offset + e0, b_in, &bar_full[st], pol);
+        if (b_rcv) tma_load_1d(s_rcv, rslot + e0 * rcv_eb, b_rcv, &bar_full[st], pol);
+        gt++;
+      }
+      if (has_rcv) rstep += sps;
+    }
+    // Never leave with bulk copies in flight: wait (time-bounded, whatever
+    // the abort flag says) until the last tile issued to every stage landed.
+    for (uint32_t st = 0; st < (uint32_t)nstages && st < gt; st++) {
+      const uint32_t last = (gt - 1 - st) / nstages * nstages + st;  // last tile issued to stage st
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar_full[st], (last / nstages) & 1u)) {
+        if (global_timer_ns() - t0 > a.timeout_ns) {
+          report_failure(header_of(a), kErrTimeout, info | (8u << 24), last);
+          break;
+        }
+      }
+    }
+  } else if (warp == 2) {
+    if (lane != 0) return;
     // ---- poster ----
     uint64_t rstep = base_recv, sstep = base_send;
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
-      if (!mbar_wait(a, &bar_done[d], use & 1u, info | (4u << 24) | i)) { sh_abort = 1; break; }
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (4u << 24) | i) ||
+          !mbar_wait(a, &bar_done[d], use & 1u, info | (4u << 24) | i)) {
+        sh_abort = 1;
+        break;
+      }
       if (sh_abort) break;
       if (row_sends(c.prim)) {
         sstep += sps;
@@ -301,26 +399,46 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
         rstep += sps;
         if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // release the slots read
       }
-      mbar_arrive(&bar_empty[d]);
+      mbar_arrive(&bar_free[d]);
     }
   } else {
     // ---- workers ----
-    const int wt = threadIdx.x - 64;
-    const T* in = reinterpret_cast<const T*>(a.send[rank]);
-    T* out = reinterpret_cast<T*>(a.recv[rank]);
-    const int64_t step_bytes = g.step_bytes;
+    const int ct = threadIdx.x - 96;
     uint64_t rstep = base_recv, sstep = base_send;
+    uint32_t gt = 0;
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
-      bool ok = mbar_wait(a, &bar_full[d], use & 1u, info | (5u << 24) | i);
-      if (!ok || sh_abort) {
+      // Gate every slice on the waiter (which the poster paces), so the
+      // workers never run more than D slices ahead, even across empty slices.
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (5u << 24) | i) || sh_abort) {
         mbar_arrive(&bar_done[d]);
+        sh_abort = 1;
         break;
       }
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
-      move_slice_any<T>(c.prim, in + c.offset, out + c.offset, rslot, sslot, c.nelem, wt, kWorkers);
+      const int ntiles = (int)div_up(c.nelem, kTileElems);
+      bool stop = false;
+      for (int k = 0; k < ntiles; k++, gt++) {
+        const uint32_t st = gt % nstages, su = gt / nstages;
+        if (!mbar_wait(a, &bar_full[st], su & 1u, info | (5u << 24) | i) || sh_abort) {
+          stop = true;
+          break;
+        }
+        const int64_t e0 = (int64_t)k * kTileElems;
+        const int ne = (int)imin(kTileElems, c.nelem - e0);
+        const char* s_in = smem + (int64_t)st * SB;
+        const char* s_rcv = s_in + kTileElems * (int)sizeof(T);
+        tile_compute_any<T>(c.prim, s_in, s_rcv, in + c.offset, out + c.offset, rslot, sslot, e0, ne, ne / P * P,
+                            ct, kComputeThreads);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+      }
       mbar_arrive(&bar_done[d]);
+      if (stop) {
+        sh_abort = 1;
+        break;
+      }
       if (row_recvs(c.prim)) rstep += sps;
       if (row_sends(c.prim)) sstep += sps;
     }
@@ -329,20 +447,43 @@ __global__ void __launch_bounds__(NT, 1) ring_simple_kernel(const __grid_constan
 
 // Host-side launch of the Simple kernel (declared in rar_launch.h).
 cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
-  constexpr int kThreads = 544;  // 2 control warps + 15 worker warps (the page's Simple blockX)
+  int device = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  static int sm_count[64] = {0};
+  sms = device < 64 ? sm_count[device] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    if (device < 64) sm_count[device] = sms;
+  }
+  // One block per SM gets the deep stage ring; grids larger than the SM
+  // count use two stages so that several blocks fit on an SM.
+  const int nstages = grid <= sms ? kMaxStages : 2;
+  const bool f32 = a.geo.dtype == kF32;
+  const int smem = nstages * (f32 ? stage_bytes<float>() : stage_bytes<uint16_t>());
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[f32 ? 0 : 1]) {
+    e = f32 ? cudaFuncSetAttribute(ring_simple_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxStages * stage_bytes<float>())
+            : cudaFuncSetAttribute(ring_simple_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxStages * stage_bytes<uint16_t>());
+    if (e != cudaSuccess) return e;
+    attr_set[f32 ? 0 : 1] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(kSimpleThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (threads_out) *threads_out = kThreads;
-  if (a.geo.dtype == kF32) return cudaLaunchKernelEx(&cfg, ring_simple_kernel<float, kThreads>, a);
-  return cudaLaunchKernelEx(&cfg, ring_simple_kernel<uint16_t, kThreads>, a);
+  if (threads_out) *threads_out = kSimpleThreads;
+  if (f32) return cudaLaunchKernelEx(&cfg, ring_simple_kernel<float>, a, nstages);
+  return cudaLaunchKernelEx(&cfg, ring_simple_kernel<uint16_t>, a, nstages);
 }
 
 }  // namespace rar
