@@ -152,14 +152,17 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 }
 // Line polls and line stores of LL / LL128: one 16-byte access each, so a
 // line's data and its flag(s) travel together ([C23] "LL：Data 与 Flag 同 Line").
-__device__ __forceinline__ uint4 ld_volatile_v4(const void* p) {
+// Strong relaxed accesses at GPU scope: every reader and writer is an SM of
+// this GPU, so they meet in L2. (The system-scope volatile form the page
+// uses, for peers across NVLink, serialises a thread's polls.)
+__device__ __forceinline__ uint4 ld_line_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.volatile.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_volatile_v4(void* p, uint4 v) {
-  asm volatile("st.volatile.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+__device__ __forceinline__ void st_line_v4(void* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
 }
@@ -303,6 +306,30 @@ __device__ __forceinline__ bool entry_check(const RingArgs& a) {
 __device__ __forceinline__ uint64_t round_up_steps(uint64_t v) {
   return (v + kSteps - 1) / kSteps * kSteps;
 }
+
+// LL128: lane geometry inside a group of 4 lines (512 bytes) moved by one
+// warp access of 16 bytes per lane. Lane l holds bytes [16l, 16l+16) of the
+// group: line l/8, 64-bit words 2(l%8) and 2(l%8)+1. Word 15 of each line is
+// its flag, held by the lane with l%8 == 7 next to payload word 14. The 480
+// payload bytes of a group are spread over the lanes so that every user
+// access stays aligned: lanes with l%8 < 7 carry group payload bytes
+// 16*(7*(l/8) + l%8) .. +16, the four flag lanes carry bytes 448 + 8*(l/8) .. +8.
+struct LL128Lane {
+  int lane;
+  bool flag_lane;
+  int piece_off;   // payload byte offset of the lane's piece inside the group
+  int piece_bytes; // 16, or 8 for flag lanes
+  __device__ __forceinline__ LL128Lane() {
+    lane = threadIdx.x & 31;
+    const int q = lane >> 3, t8 = lane & 7;
+    flag_lane = (t8 == 7);
+    piece_off = flag_lane ? 448 + 8 * q : 16 * (7 * q + t8);
+    piece_bytes = flag_lane ? 8 : 16;
+  }
+};
+
+
+__device__ __forceinline__ uint64_t ll128_flag_of(const uint4& v) { return ((uint64_t)v.w << 32) | v.z; }
 
 // bf16 helpers: widening is exact (a bf16 is the upper half of a binary32);
 // narrowing is round-to-nearest-even by the hardware conversion.

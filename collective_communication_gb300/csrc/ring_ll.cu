@@ -121,7 +121,7 @@ __device__ __forceinline__ bool ll_poll(const RingArgs& a, const char* p, uint32
   while (!ll_ready(v, flag)) {
     if (*sh_abort) return false;
     if (sp.poll(a, info, flag)) { *sh_abort = 1; return false; }
-    v = ld_volatile_v4(p);
+    v = ld_line_v4(p);
   }
   return true;
 }
@@ -132,7 +132,7 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
                                          uint64_t info) {
   constexpr int K = LLUnit<T>::kElems;
   constexpr int PL = LLUnit<T>::kPartLines;
-  constexpr int UL = 4;
+  constexpr int UL = 1;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvFinal = PRIM == kRecvCopySend || PRIM == kRecv;
@@ -151,7 +151,7 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
       if (unit < nunits) {
         if (kRecvPartial || kRecvFinal) {
 #pragma unroll
-          for (int l = 0; l < RL; l++) rl[u][l] = ld_volatile_v4(rslot + (unit * RL + l) * 16);
+          for (int l = 0; l < RL; l++) rl[u][l] = ld_line_v4(rslot + (unit * RL + l) * 16);
         }
         if (kIn) load_input_n<T, K>(in + unit * K, (int)imin(K, nelem - unit * K), x[u]);
       }
@@ -190,7 +190,7 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
       if (kSendPartial) {
 #pragma unroll
         for (int l = 0; l < PL; l++)
-          st_volatile_v4(sslot + (unit * PL + l) * 16,
+          st_line_v4(sslot + (unit * PL + l) * 16,
                          make_uint4(__float_as_uint(v[2 * l]), sflag, __float_as_uint(v[2 * l + 1]), sflag));
       } else {
         // final values: 8 bytes of T
@@ -203,7 +203,7 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
           f = make_uint2(round_bf16_pair(v[0], v[1]), round_bf16_pair(v[2], v[3]));  // rounded once
         }
         if (kOut) store_out_n<T>(out + unit * K, kv, K, make_uint4(f.x, f.y, 0u, 0u));
-        if (kSendFinal) st_volatile_v4(sslot + unit * 16, make_uint4(f.x, sflag, f.y, sflag));
+        if (kSendFinal) st_line_v4(sslot + unit * 16, make_uint4(f.x, sflag, f.y, sflag));
       }
     }
   }
@@ -212,7 +212,6 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
 // ---------------------------------------------------------------------------
 // LL128
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t ll128_flag_of(const uint4& v) { return ((uint64_t)v.w << 32) | v.z; }
 
 // Warp-uniform wait until every flag lane of the group sees `flag`.
 __device__ __forceinline__ bool ll128_poll(const RingArgs& a, const char* p, uint64_t flag, bool flag_lane, uint4& v,
@@ -226,24 +225,9 @@ __device__ __forceinline__ bool ll128_poll(const RingArgs& a, const char* p, uin
     if (lane == 0 && !stop && sp.poll(a, info, flag)) { *sh_abort = 1; stop = 1; }
     stop = __shfl_sync(kFullMask, stop, 0);
     if (stop) return false;
-    v = ld_volatile_v4(p);
+    v = ld_line_v4(p);
   }
 }
-
-// Lane geometry inside a 4-line group.
-struct LL128Lane {
-  int lane;
-  bool flag_lane;
-  int piece_off;   // payload byte offset of the lane's piece inside the group
-  int piece_bytes; // 16, or 8 for flag lanes
-  __device__ __forceinline__ LL128Lane() {
-    lane = threadIdx.x & 31;
-    const int q = lane >> 3, t8 = lane & 7;
-    flag_lane = (t8 == 7);
-    piece_off = flag_lane ? 448 + 8 * q : 16 * (7 * q + t8);
-    piece_bytes = flag_lane ? 8 : 16;
-  }
-};
 
 // Same payload element size on both sides (all rows except bf16's owner row).
 template <typename T, int PRIM, int NT>
@@ -251,7 +235,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
                                             int64_t nelem, uint64_t rflag, uint64_t sflag, volatile int* sh_abort,
                                             uint64_t info) {
   constexpr int NW = NT / 32;
-  constexpr int UG = 2;
+  constexpr int UG = 1;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kHasRecv = PRIM != kSend;
@@ -273,7 +257,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
     for (int u = 0; u < UG; u++) {
       const int64_t g = g0 + (int64_t)u * NW;
       if (g < ngroups) {
-        if (kHasRecv) rv[u] = ld_volatile_v4(rslot + g * 512 + 16 * L.lane);
+        if (kHasRecv) rv[u] = ld_line_v4(rslot + g * 512 + 16 * L.lane);
         if (kIn) {
           const int64_t e0 = (g * 480 + L.piece_off) / EB;
           const int kv = (int)imax(0, imin(kmax, nelem - e0));
@@ -319,7 +303,7 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
           pay.z = (uint32_t)sflag;
           pay.w = (uint32_t)(sflag >> 32);
         }
-        st_volatile_v4(sslot + g * 512 + 16 * L.lane, pay);
+        st_line_v4(sslot + g * 512 + 16 * L.lane, pay);
       }
       (void)KMAX;
     }
@@ -346,7 +330,7 @@ __device__ __forceinline__ void ll128_owner_bf16(const RingArgs& a, const uint16
       const int64_t gr = 2 * gs + h;
       if (gr >= nrecv) break;  // uniform
       const char* rp = rslot + gr * 512 + 16 * L.lane;
-      uint4 rv = ld_volatile_v4(rp);
+      uint4 rv = ld_line_v4(rp);
       const int kmax = L.piece_bytes / 4;
       const int64_t e0 = (gr * 480 + L.piece_off) / 4;
       const int kv = (int)imax(0, imin(kmax, nelem - e0));
@@ -379,7 +363,7 @@ __device__ __forceinline__ void ll128_owner_bf16(const RingArgs& a, const uint16
         pay.z = (uint32_t)sflag;
         pay.w = (uint32_t)(sflag >> 32);
       }
-      st_volatile_v4(sslot + gs * 512 + 16 * L.lane, pay);
+      st_line_v4(sslot + gs * 512 + 16 * L.lane, pay);
     }
     __syncwarp();
   }
@@ -398,6 +382,46 @@ __device__ __noinline__ bool wait_credit(const RingArgs& a, ConnCounters* cs, ui
     const uint64_t h2 = *head_seen > base_send ? *head_seen : base_send;
     if (h2 + kSteps >= step + 1) return true;
     if (sp.poll(a, info, step + 1)) return false;
+  }
+}
+
+// Pacing (thread 0, before a large step): wait until the LAST line of the
+// step carries the step's flag. All ranks run at the same speed on one GPU, so
+// without this a receiver chases its sender line by line and most of its
+// early loads see stale flags, each costing another L2 round trip. The wait
+// is only a hint about progress: every line is still accepted by its own flag
+// alone. Steps that fit in one pass of the block (<= one unit per thread for
+// LL, <= one group per warp for LL128) keep pure line-by-line streaming.
+template <typename T, int PROTO, int NT>
+__device__ __noinline__ bool pace_wait(const RingArgs& a, const char* rslot, int prim, int64_t nelem, uint64_t rstep,
+                                       uint64_t info) {
+  if (nelem <= 0 || !row_recvs(prim)) return true;
+  const bool partial = row_recvs_partial(prim);
+  Spin sp;
+  if (PROTO == kLL) {
+    constexpr int K = LLUnit<T>::kElems;
+    const int64_t nunits = div_up(nelem, K);
+    if (nunits <= NT) return true;
+    const int64_t lines = nunits * (partial ? LLUnit<T>::kPartLines : 1);
+    const char* p = rslot + (lines - 1) * 16;
+    const uint32_t flag = (uint32_t)(rstep + 1);
+    uint4 v = ld_line_v4(p);
+    while (!ll_ready(v, flag)) {
+      if (sp.poll(a, info, flag)) return false;
+      v = ld_line_v4(p);
+    }
+    return true;
+  } else {
+    const int64_t ngroups = div_up(nelem * (partial ? 4 : (int64_t)sizeof(T)), 480);
+    if (ngroups <= NT / 32) return true;
+    const uint64_t* p = reinterpret_cast<const uint64_t*>(rslot + (4 * (ngroups - 1) + 3) * 128 + 120);
+    const uint64_t flag = rstep + 1;
+    while (true) {
+      uint64_t f;
+      f = ld_relaxed_u64(p);
+      if (f == flag) return true;
+      if (sp.poll(a, info, flag)) return false;
+    }
   }
 }
 
@@ -470,9 +494,13 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   uint64_t rstep = sh_base_recv, sstep = base_send, head_seen = 0;
   SliceCursor c;
   cursor_begin(g, dense, ring_idx, c);
-  if (threadIdx.x == 0 && c.valid && row_sends(c.prim) &&
-      !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24)))
-    sh_abort = 1;
+  if (threadIdx.x == 0 && c.valid) {
+    if (row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24)))
+      sh_abort = 1;
+    else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(rstep % kSteps) * step_bytes, c.prim, c.nelem, rstep,
+                                      info | (9u << 24)))
+      sh_abort = 1;
+  }
   __syncthreads();
   uint32_t i = 0;
   while (c.valid && !sh_abort) {
@@ -483,10 +511,15 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
     SliceCursor nx = c;
     cursor_next(g, nx);
     const uint64_t nsstep = sstep + (row_sends(c.prim) ? 1 : 0);
-    // credit for the next step, taken while the block finishes this one
-    if (threadIdx.x == 0 && nx.valid && row_sends(nx.prim) && !sh_abort &&
-        !wait_credit(a, cs, base_send, nsstep, &head_seen, info | (3u << 24) | (i + 1)))
-      sh_abort = 1;
+    const uint64_t nrstep = rstep + (row_recvs(c.prim) ? 1 : 0);
+    // credit and pacing for the next step, taken while the block finishes this one
+    if (threadIdx.x == 0 && nx.valid && !sh_abort) {
+      if (row_sends(nx.prim) && !wait_credit(a, cs, base_send, nsstep, &head_seen, info | (3u << 24) | (i + 1)))
+        sh_abort = 1;
+      else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(nrstep % kSteps) * step_bytes, nx.prim, nx.nelem,
+                                        nrstep, info | (9u << 24) | (i + 1)))
+        sh_abort = 1;
+    }
     __syncthreads();
     if (threadIdx.x == 0 && row_recvs(c.prim) && !sh_abort && a.fault != kFaultDropHead)
       st_relaxed_u64(&cr->head, rstep + 1);  // every thread has read this step's lines
@@ -499,9 +532,403 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   if (threadIdx.x == 0 && !sh_abort) st_relaxed_u64(&cs->tail, sstep);
 }
 
+// ---------------------------------------------------------------------------
+// LL128, bulk form: the same lines, flags and head credits, with the loads of
+// large steps moved onto the TMA engine (used when chunks span at least one
+// tile). Roles as in the Simple kernel:
+//   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1) and a
+//                   pacing wait for the step's last line flag; arrives ready[i % D].
+//   warp 1, lane 0  loader: per tile of kL8TileElems elements, bulk copies of
+//                   the tile's received lines and user input into a smem stage.
+//   warps 3..10     workers: per 4-line group, check every line's flag in
+//                   shared memory (a line that is not yet there is re-polled
+//                   from global memory until its flag matches), reduce, store
+//                   the output and write the outgoing lines, one warp access
+//                   per 4 lines, flag word included.
+//   warp 2, lane 0  poster: publishes the head once the step's lines are read.
+// A line is accepted only by its own flag, exactly as in the polling form.
+// ---------------------------------------------------------------------------
+constexpr int kL8TileElems = 3840;   // 32 groups of binary32 payload, 16 groups of bf16 payload
+constexpr int kL8TileGroups = 32;
+constexpr int kL8Warps = 8;
+constexpr int kL8WorkThreads = 32 * kL8Warps;
+constexpr int kL8Threads = 32 * 3 + kL8WorkThreads;
+constexpr int kL8Depth = 4;
+constexpr int kL8MaxStages = 8;
+constexpr int kL8SmemBudget = 200 * 1024;
+
+template <typename T>
+__host__ __device__ constexpr int l8_stage_bytes() { return kL8TileGroups * 512 + kL8TileElems * (int)sizeof(T); }
+template <typename T>
+__host__ __device__ constexpr int l8_max_stages() {
+  return kL8SmemBudget / l8_stage_bytes<T>() < kL8MaxStages ? kL8SmemBudget / l8_stage_bytes<T>() : kL8MaxStages;
+}
+
+// Input element j of the tile (binary32): from the staged prefix, or from
+// global memory past it (the last < 16 bytes of a slice).
+template <typename T>
+__device__ __forceinline__ float l8_input(const char* s_in, const T* g_tile, int j, int covered) {
+  if (j < covered) {
+    if constexpr (sizeof(T) == 4) return reinterpret_cast<const float*>(s_in)[j];
+    else return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(s_in)[j] << 16);
+  }
+  if constexpr (sizeof(T) == 4) return __uint_as_float(ld_cg_u32(g_tile + j));
+  uint16_t h;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(g_tile + j) : "memory");
+  return __uint_as_float((uint32_t)h << 16);
+}
+
+// Check a group's flags as staged; re-poll stale lines from global memory.
+__device__ __forceinline__ bool l8_accept(const RingArgs& a, uint4& v, const char* gline, uint64_t flag, bool flag_lane,
+                                          volatile int* sh_abort, uint64_t info) {
+  const bool need = flag_lane && ll128_flag_of(v) != flag;
+  if (!__any_sync(kFullMask, need)) return true;
+  v = ld_line_v4(gline);
+  return ll128_poll(a, gline, flag, flag_lane, v, sh_abort, info);
+}
+
+template <typename T, int PRIM>
+__device__ __forceinline__ void l8_tile_same_layout(const RingArgs& a, const char* s_lines, const char* s_in,
+                                                    const T* g_in_tile, T* g_out_tile, const char* g_rlines,
+                                                    char* g_slines, int ne, int covered, uint64_t rflag, uint64_t sflag,
+                                                    volatile int* sh_abort, uint64_t info, int w) {
+  constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
+  constexpr bool kHasRecv = PRIM != kSend;
+  constexpr bool kHasSend = PRIM != kRecv;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
+  constexpr int EB = (PRIM == kSend || kRecvPartial) ? 4 : (int)sizeof(T);
+  const LL128Lane L;
+  const int kmax = L.piece_bytes / EB;
+  const int ng = (int)div_up((int64_t)ne * EB, 480);
+  for (int gl = w; gl < ng; gl += kL8Warps) {
+    uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+    bool ok = true;
+    if (kHasRecv) {
+      rv = *reinterpret_cast<const uint4*>(s_lines + gl * 512 + 16 * L.lane);
+      ok = l8_accept(a, rv, g_rlines + gl * 512 + 16 * L.lane, rflag, L.flag_lane, sh_abort, info);
+    }
+    if (!ok) return;  // uniform across the warp
+    const int el = (gl * 480 + L.piece_off) / EB;
+    const int kv = (int)imax(0, imin(kmax, ne - el));
+    uint4 pay;
+    if (kRecvPartial || PRIM == kSend) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (kRecvPartial) {
+        v[0] = __uint_as_float(rv.x); v[1] = __uint_as_float(rv.y);
+        v[2] = __uint_as_float(rv.z); v[3] = __uint_as_float(rv.w);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        if (j < kv) {
+          const float x = l8_input<T>(s_in, g_in_tile, el + j, covered);
+          v[j] = kRecvPartial ? __fadd_rn(v[j], x) : x;
+        } else {
+          v[j] = 0.f;
+        }
+      }
+      pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+    } else {
+      pay = rv;  // final values pass through unchanged
+    }
+    if (kOut && kv > 0) store_out_n<T>(g_out_tile + el, kv, kmax, pay);
+    if (kHasSend) {
+      if (L.flag_lane) {
+        pay.z = (uint32_t)sflag;
+        pay.w = (uint32_t)(sflag >> 32);
+      }
+      st_line_v4(g_slines + gl * 512 + 16 * L.lane, pay);
+    }
+  }
+}
+
+// bf16 owner row: binary32 partial sums in (120 elements per group), bf16
+// finals out (240 elements per group). The finals are written over the staged
+// bf16 input (each element by the lane that read it), then re-read in the
+// send layout after a barrier of the worker warps.
+__device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char* s_lines, char* s_in,
+                                                   const uint16_t* g_in_tile, uint16_t* g_out_tile,
+                                                   const char* g_rlines, char* g_slines, int ne, int covered,
+                                                   uint64_t rflag, uint64_t sflag, volatile int* sh_abort,
+                                                   uint64_t info, int w, uint64_t* bar_fin, uint32_t* fin_uses) {
+  const LL128Lane L;
+  uint16_t* fin = reinterpret_cast<uint16_t*>(s_in);
+  const int ngr = (int)div_up((int64_t)ne * 4, 480), ngs = (int)div_up((int64_t)ne * 2, 480);
+  bool ok = true;
+  for (int gl = w; gl < ngr && ok; gl += kL8Warps) {
+    uint4 rv = *reinterpret_cast<const uint4*>(s_lines + gl * 512 + 16 * L.lane);
+    ok = l8_accept(a, rv, g_rlines + gl * 512 + 16 * L.lane, rflag, L.flag_lane, sh_abort, info);
+    if (!ok) break;
+    const int kmax = L.piece_bytes / 4;
+    const int el = (gl * 480 + L.piece_off) / 4;
+    const int kv = (int)imax(0, imin(kmax, ne - el));
+    const float p[4] = {__uint_as_float(rv.x), __uint_as_float(rv.y), __uint_as_float(rv.z), __uint_as_float(rv.w)};
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; j++)
+      if (j < kv) v[j] = __fadd_rn(p[j], l8_input<uint16_t>(s_in, g_in_tile, el + j, covered));
+    const uint4 wv = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), 0u, 0u);  // rounded once
+    if (kv > 0) store_out_n<uint16_t>(g_out_tile + el, kv, kmax, wv);
+    for (int j = 0; j < kv; j++) fin[el + j] = (uint16_t)((j < 2 ? wv.x : wv.y) >> ((j & 1) * 16));
+  }
+  // every worker warp passes this barrier once per owner tile, on every path;
+  // the wait is bounded like every other wait of the kernel
+  __syncwarp();
+  if (L.lane == 0) mbar_arrive(bar_fin);
+  const bool passed = mbar_wait(a, bar_fin, (*fin_uses) & 1u, info);
+  (*fin_uses)++;
+  if (!passed || *sh_abort) {
+    *sh_abort = 1;
+    return;
+  }
+  for (int gl = w; gl < ngs; gl += kL8Warps) {
+    const int kmax = L.piece_bytes / 2;
+    const int el = (gl * 480 + L.piece_off) / 2;
+    const int kv = (int)imax(0, imin(kmax, ne - el));
+    uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+      if (j < kv) wd[j >> 1] |= (uint32_t)fin[el + j] << ((j & 1) * 16);
+    uint4 pay = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    if (L.flag_lane) {
+      pay.z = (uint32_t)sflag;
+      pay.w = (uint32_t)(sflag >> 32);
+    }
+    st_line_v4(g_slines + gl * 512 + 16 * L.lane, pay);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const char* s_lines, char* s_in,
+                                            const T* g_in_tile, T* g_out_tile, const char* g_rlines, char* g_slines,
+                                            int ne, int covered, uint64_t rflag, uint64_t sflag,
+                                            volatile int* sh_abort, uint64_t info, int w, uint64_t* bar_fin,
+                                            uint32_t* fin_uses) {
+  switch (prim) {
+    case kSend:
+      l8_tile_same_layout<T, kSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag,
+                                    sflag, sh_abort, info, w);
+      break;
+    case kRecvReduceSend:
+      l8_tile_same_layout<T, kRecvReduceSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne,
+                                              covered, rflag, sflag, sh_abort, info, w);
+      break;
+    case kRecvReduceCopySend:
+      if constexpr (sizeof(T) == 4)
+        l8_tile_same_layout<T, kRecvReduceCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne,
+                                                    covered, rflag, sflag, sh_abort, info, w);
+      else
+        l8_tile_owner_bf16(a, s_lines, s_in, reinterpret_cast<const uint16_t*>(g_in_tile),
+                           reinterpret_cast<uint16_t*>(g_out_tile), g_rlines, g_slines, ne, covered, rflag, sflag,
+                           sh_abort, info, w, bar_fin, fin_uses);
+      break;
+    case kRecvCopySend:
+      l8_tile_same_layout<T, kRecvCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                            rflag, sflag, sh_abort, info, w);
+      break;
+    default:
+      l8_tile_same_layout<T, kRecv>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag,
+                                    sflag, sh_abort, info, w);
+      break;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __grid_constant__ RingArgs a,
+                                                                        int nstages) {
+  extern __shared__ __align__(128) char smem[];
+  __shared__ uint64_t bar_ready[kL8Depth], bar_done[kL8Depth], bar_free[kL8Depth];
+  __shared__ uint64_t bar_full[kL8MaxStages], bar_empty[kL8MaxStages], bar_fin;
+  __shared__ volatile int sh_abort;
+  __shared__ int sh_chan;
+  __shared__ uint64_t sh_base_send, sh_base_recv;
+  constexpr int P = 16 / (int)sizeof(T);
+  constexpr int SB = l8_stage_bytes<T>();
+
+  const Geometry& g = a.geo;
+  if (threadIdx.x == 0) sh_chan = -1;
+  __syncthreads();
+  int rank, dense;
+  map_block(a, &rank, &dense, &sh_chan);
+  __syncthreads();
+  const int N = g.nranks;
+  const int ring_idx = a.ring_index[rank];
+  const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
+  ConnCounters* cs = conn_at(a, dense, e_send);
+  ConnCounters* cr = conn_at(a, dense, e_recv);
+  char* fifo_send = fifo_at(a, dense, e_send);
+  const char* fifo_recv = fifo_at(a, dense, e_recv);
+  if (threadIdx.x == 0) {
+    sh_abort = entry_check(a) ? 0 : 1;
+    for (int d = 0; d < kL8Depth; d++) {
+      mbar_init(&bar_ready[d], 1);
+      mbar_init(&bar_done[d], kL8WorkThreads);
+      mbar_init(&bar_free[d], 1);
+    }
+    for (int st = 0; st < kL8MaxStages; st++) {
+      mbar_init(&bar_full[st], 1);
+      mbar_init(&bar_empty[st], kL8Warps);
+    }
+    mbar_init(&bar_fin, kL8Warps);
+    // Both counters belong to this block and equal the previous call's final step.
+    sh_base_send = ld_relaxed_u64(&cs->tail);
+    sh_base_recv = ld_relaxed_u64(&cr->head);
+    reinterpret_cast<uint8_t*>(a.ws + kTraceOffset)[blockIdx.x] = (uint8_t)sh_chan;
+  }
+  __syncthreads();
+  if (sh_abort) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t base_send = sh_base_send, base_recv = sh_base_recv;
+  const uint64_t info = ((uint64_t)blockIdx.x << 32);
+  const int64_t step_bytes = g.step_bytes;
+  const T* in = reinterpret_cast<const T*>(a.send[rank]);
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
+  SliceCursor c;
+  cursor_begin(g, dense, ring_idx, c);
+
+  if (warp == 0) {
+    if (lane != 0) return;
+    // ---- waiter ----
+    uint64_t rstep = base_recv, sstep = base_send, head_seen = 0;
+    for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
+      const uint32_t d = i % kL8Depth, use = i / kL8Depth;
+      if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
+      if (!sh_abort && row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24) | i))
+        sh_abort = 1;
+      if (!sh_abort && c.nelem > 0 && row_recvs(c.prim)) {
+        const int eb = row_recvs_partial(c.prim) ? 4 : (int)sizeof(T);
+        const int64_t ngroups = div_up(c.nelem * eb, 480);
+        const uint64_t* p =
+            reinterpret_cast<const uint64_t*>(fifo_recv + (int64_t)(rstep % kSteps) * step_bytes +
+                                              (4 * (ngroups - 1) + 3) * 128 + 120);
+        Spin sp;
+        while (ld_relaxed_u64(p) != rstep + 1) {
+          if (sp.poll(a, info | (9u << 24) | i, rstep + 1)) { sh_abort = 1; break; }
+        }
+      }
+      mbar_arrive(&bar_ready[d]);
+      if (sh_abort) break;
+      if (row_recvs(c.prim)) rstep++;
+      if (row_sends(c.prim)) sstep++;
+    }
+  } else if (warp == 1) {
+    if (lane != 0) return;
+    // ---- loader ----
+    const uint64_t pol = l2_policy_evict_first();
+    uint64_t rstep = base_recv;
+    uint32_t gt = 0;
+    for (uint32_t i = 0; c.valid && !sh_abort; i++, cursor_next(g, c)) {
+      const uint32_t d = i % kL8Depth, use = i / kL8Depth;
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) {
+        sh_abort = 1;
+        break;
+      }
+      const int prim = c.prim;
+      const bool has_in = prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend;
+      const bool has_rcv = row_recvs(prim);
+      const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
+      const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
+      if (has_rcv) fence_proxy_async_global();
+      const int ntiles = (int)div_up(c.nelem, kL8TileElems);
+      for (int k = 0; k < ntiles; k++) {
+        const uint32_t st = gt % nstages, su = gt / nstages;
+        if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
+          sh_abort = 1;
+          break;
+        }
+        const int64_t e0 = (int64_t)k * kL8TileElems;
+        const int ne = (int)imin(kL8TileElems, c.nelem - e0);
+        const int covered = ne / P * P;
+        const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
+        const uint32_t b_rcv = has_rcv ? (uint32_t)div_up((int64_t)ne * eb, 480) * 512u : 0u;
+        char* s_lines = smem + (int64_t)st * SB;
+        char* s_in = s_lines + kL8TileGroups * 512;
+        mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
+        if (b_rcv) tma_load_1d(s_lines, rslot + e0 * eb / 480 * 512, b_rcv, &bar_full[st], pol);
+        if (b_in) tma_load_1d(s_in, in + c.offset + e0, b_in, &bar_full[st], pol);
+        gt++;
+      }
+      if (has_rcv) rstep++;
+    }
+    for (uint32_t st = 0; st < (uint32_t)nstages && st < gt; st++) {
+      const uint32_t last = (gt - 1 - st) / nstages * nstages + st;
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar_full[st], (last / nstages) & 1u)) {
+        if (global_timer_ns() - t0 > a.timeout_ns) {
+          report_failure(header_of(a), kErrTimeout, info | (8u << 24), last);
+          break;
+        }
+      }
+    }
+  } else if (warp == 2) {
+    if (lane != 0) return;
+    // ---- poster ----
+    uint64_t rstep = base_recv, sstep = base_send;
+    bool aborted = false;
+    for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
+      const uint32_t d = i % kL8Depth, use = i / kL8Depth;
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (4u << 24) | i) ||
+          !mbar_wait(a, &bar_done[d], use & 1u, info | (4u << 24) | i) || sh_abort) {
+        sh_abort = 1;
+        aborted = true;
+        break;
+      }
+      if (row_recvs(c.prim)) {
+        rstep++;
+        if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // every line of the step was read
+      }
+      if (row_sends(c.prim)) sstep++;
+      mbar_arrive(&bar_free[d]);
+    }
+    if (!aborted) st_relaxed_u64(&cs->tail, sstep);  // the sender's step count carries over to the next call
+  } else {
+    // ---- workers ----
+    const int w = warp - 3;
+    uint64_t rstep = base_recv, sstep = base_send;
+    uint32_t gt = 0, fin_uses = 0;
+    for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
+      const uint32_t d = i % kL8Depth, use = i / kL8Depth;
+      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (5u << 24) | i) || sh_abort) {
+        mbar_arrive(&bar_done[d]);
+        sh_abort = 1;
+        break;
+      }
+      const int eb_r = row_recvs_partial(c.prim) ? 4 : (int)sizeof(T);
+      const int eb_s = row_sends_partial(c.prim) ? 4 : (int)sizeof(T);
+      const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
+      char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
+      const int ntiles = (int)div_up(c.nelem, kL8TileElems);
+      bool stop = false;
+      for (int k = 0; k < ntiles; k++, gt++) {
+        const uint32_t st = gt % nstages, su = gt / nstages;
+        if (!mbar_wait(a, &bar_full[st], su & 1u, info | (5u << 24) | i)) sh_abort = 1;
+        const int64_t e0 = (int64_t)k * kL8TileElems;
+        const int ne = (int)imin(kL8TileElems, c.nelem - e0);
+        char* s_lines = smem + (int64_t)st * SB;
+        char* s_in = s_lines + kL8TileGroups * 512;
+        // the tile runs on every path so that the workers' barrier counts match
+        l8_tile_any<T>(c.prim, a, s_lines, s_in, in + c.offset + e0, out + c.offset + e0,
+                       rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne, ne / P * P,
+                       rstep + 1, sstep + 1, &sh_abort, info | (10u << 24) | i, w, &bar_fin, &fin_uses);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_empty[st]);
+        if (sh_abort) {
+          stop = true;
+          break;
+        }
+      }
+      mbar_arrive(&bar_done[d]);
+      if (stop) break;
+      if (row_recvs(c.prim)) rstep++;
+      if (row_sends(c.prim)) sstep++;
+    }
+  }
+}
+
 cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
-  constexpr int kThreadsLL = 512;     // the page's LL blockX
-  constexpr int kThreadsLL128 = 640;  // the page's LL128 blockX (20 warps)
+  constexpr int kThreadsLL = 1024;     // one line unit per thread, many warps
+  constexpr int kThreadsLL128 = 1024;  // one 4-line group per warp pass, many warps
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -517,6 +944,31 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
     if (threads_out) *threads_out = kThreadsLL;
     return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLL>, a)
                : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLL>, a);
+  }
+  // LL128: the bulk form once the first loop's chunks span a whole tile,
+  // the polling form (lowest latency) for smaller messages.
+  const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
+  int device = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return e;
+  if (first_chunk >= kL8TileElems && grid <= sms) {
+    const int nstages = f32 ? l8_max_stages<float>() : l8_max_stages<uint16_t>();
+    const int smem = nstages * (f32 ? l8_stage_bytes<float>() : l8_stage_bytes<uint16_t>());
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[f32 ? 0 : 1]) {
+      e = f32 ? cudaFuncSetAttribute(ring_ll128_bulk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+              : cudaFuncSetAttribute(ring_ll128_bulk_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
+      if (e != cudaSuccess) return e;
+      attr_set[f32 ? 0 : 1] = true;
+    }
+    cfg.blockDim = dim3(kL8Threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    if (threads_out) *threads_out = kL8Threads;
+    return f32 ? cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<float>, a, nstages)
+               : cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<uint16_t>, a, nstages);
   }
   cfg.blockDim = dim3(kThreadsLL128);
   if (threads_out) *threads_out = kThreadsLL128;

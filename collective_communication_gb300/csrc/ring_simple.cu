@@ -229,14 +229,19 @@ __device__ __forceinline__ void tile_compute_any(int prim, const char* s_in, con
   }
 }
 
-constexpr int kTileElems = 4096;    // elements per bulk-copied tile
-constexpr int kMaxStages = 6;
+constexpr int kTileElems = 8192;    // elements per bulk-copied tile
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 200 * 1024;  // dynamic shared memory for the stage ring
 constexpr int kComputeWarps = 8;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kSimpleThreads = 32 * 3 + kComputeThreads;  // waiter, loader, poster + workers
 
 template <typename T>
 __host__ __device__ constexpr int stage_bytes() { return kTileElems * ((int)sizeof(T) + 4); }
+template <typename T>
+__host__ __device__ constexpr int max_stages() {
+  return kSmemBudget / stage_bytes<T>() < kMaxStages ? kSmemBudget / stage_bytes<T>() : kMaxStages;
+}
 
 __device__ __forceinline__ bool recv_is_partial(int prim) { return row_recvs_partial(prim); }
 
@@ -459,15 +464,16 @@ cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream,
   }
   // One block per SM gets the deep stage ring; grids larger than the SM
   // count use two stages so that several blocks fit on an SM.
-  const int nstages = grid <= sms ? kMaxStages : 2;
   const bool f32 = a.geo.dtype == kF32;
+  const int deep = f32 ? max_stages<float>() : max_stages<uint16_t>();
+  const int nstages = grid <= sms ? deep : 2;
   const int smem = nstages * (f32 ? stage_bytes<float>() : stage_bytes<uint16_t>());
   static bool attr_set[2] = {false, false};
   if (!attr_set[f32 ? 0 : 1]) {
     e = f32 ? cudaFuncSetAttribute(ring_simple_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kMaxStages * stage_bytes<float>())
+                                   max_stages<float>() * stage_bytes<float>())
             : cudaFuncSetAttribute(ring_simple_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kMaxStages * stage_bytes<uint16_t>());
+                                   max_stages<uint16_t>() * stage_bytes<uint16_t>());
     if (e != cudaSuccess) return e;
     attr_set[f32 ? 0 : 1] = true;
   }

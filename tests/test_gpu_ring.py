@@ -229,3 +229,74 @@ def test_sparse_mask_size_sweep(case):
         assert_bit_exact(got, oracle_full(case, x))
     else:
         _run_large(case, nsamples=50000)
+
+
+# ---------------------------------------------------------------------------
+# LL128: the bulk (TMA-staged) form for chunks of at least one 3840-element
+# tile, the polling form below that; both must give the oracle's bytes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("n,count,mask", [(2, 3840 * 3 + 5, 0b1), (3, 100003, 0b11), (5, 250001, 0b100101)])
+def test_ll128_bulk_form(n, count, mask, dtype, in_place):
+    case = gen.RingCase("ll128bulk", n, gen.ring_permutation(n, count % 97), mask, "LL128", count, dtype, "normal",
+                        count % 1000, 0, 4)
+    x = case.inputs()
+    want = oracle_full(case, x)
+    _, got, _ = run_ring(case, x=x, in_place=in_place)
+    assert_bit_exact(got, want)
+
+
+def test_ll128_forms_alternate_on_one_workspace():
+    ws = B.Workspace(4, 0b11, "LL128", 0)
+    for k, count in enumerate([1000, 200003, 777, 150000, 3, 300001]):
+        dtype = "bf16" if k % 2 else "f32"
+        case = gen.RingCase("alt", 4, gen.RING_0231, 0b11, "LL128", count, dtype, "normal", 70 + k, 0, 4)
+        x, got, _ = run_ring(case, workspace=ws)
+        assert_bit_exact(got, oracle_full(case, x))
+
+
+def test_too_many_blocks_is_refused():
+    """32 ranks x 8 channels = 256 blocks cannot all be resident on 152 SMs:
+    the cooperative launch is refused with a status, nothing hangs."""
+    n, mask, count = 32, 0xFF, 4096
+    x = gen.draw("normal", n, count, 1)
+    _, send = to_device(x, "f32")
+    _, recv = guarded_outputs(n, count, "f32")
+    ws = B.Workspace(n, mask, "Simple", 65536)
+    with pytest.raises(B.RarError) as e:
+        B.allreduce(send, recv, list(range(n)), mask, "Simple", ws, 65536, 4)
+    assert e.value.status == B.Status.ERR_CORESIDENCY
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("proto,count,bs", [("Simple", 200000, 65536), ("LL", 200000, 0),
+                                           ("LL128", 20000, 65536), ("LL128", 400000, 131072)])
+def test_dropped_head_times_out_and_recovers(proto, count, bs):
+    """Failure detection without a GPU fault: with the receivers' head
+    updates dropped, every sender runs out of credit after NCCL_STEPS steps;
+    its bounded wait expires, the block raises the workspace's abort flag,
+    every block leaves, the launch completes and the status reads TIMEOUT.
+    Re-initialising the workspace restores normal, bit-exact operation. The
+    sizes give every connection more than NCCL_STEPS steps; the two LL128
+    cases use the polling and the bulk form."""
+    case = gen.RingCase("fault", 4, gen.RING_0231, 0b11, proto, count, "f32", "normal", 8, bs, 4)
+    x = case.inputs()
+    _, send = to_device(x, "f32")
+    _, recv = guarded_outputs(4, count, "f32")
+    ws = B.Workspace(4, 0b11, proto, bs)
+    B.set_spin_timeout_ns(200_000_000)
+    try:
+        B.debug_set_fault(1)
+        B.allreduce(send, recv, case.ring, case.mask, proto, ws, bs, 4)
+        assert B.get_status(ws) == B.Status.ERR_TIMEOUT
+        B.debug_set_fault(0)
+        # the workspace stays aborted until it is initialised again
+        B.allreduce(send, recv, case.ring, case.mask, proto, ws, bs, 4)
+        assert B.get_status(ws) == B.Status.ERR_ABORT
+    finally:
+        B.debug_set_fault(0)
+        B.set_spin_timeout_ns(5_000_000_000)
+    ws.init()
+    x2, got, _ = run_ring(case, workspace=ws)
+    assert_bit_exact(got, oracle_full(case, x2))
