@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 //                   pacing wait for the step's last line flag; arrives ready[i % D].
 //   warp 1, lane 0  loader: per tile of kL8TileElems elements, bulk copies of
 //                   the tile's received lines and user input into a smem stage.
-//   warps 3..10     workers: per 4-line group, check every line's flag in
+//   warps 3..18     workers: per 4-line group, check every line's flag in
 //                   shared memory (a line that is not yet there is re-polled
 //                   from global memory until its flag matches), reduce, store
 //                   the output and write the outgoing lines, one warp access
@@ -548,9 +548,10 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 //   warp 2, lane 0  poster: publishes the head once the step's lines are read.
 // A line is accepted only by its own flag, exactly as in the polling form.
 // ---------------------------------------------------------------------------
-constexpr int kL8TileElems = 3840;   // 32 groups of binary32 payload, 16 groups of bf16 payload
-constexpr int kL8TileGroups = 32;
-constexpr int kL8Warps = 8;
+constexpr int kL8TileElems = 7680;   // 64 groups of binary32 payload, 32 groups of bf16 payload
+constexpr int kL8TileGroups = 64;
+constexpr int kL8BulkMinChunk = 3840;  // chunks at least this long take the bulk form
+constexpr int kL8Warps = 16;
 constexpr int kL8WorkThreads = 32 * kL8Warps;
 constexpr int kL8Threads = 32 * 3 + kL8WorkThreads;
 constexpr int kL8Depth = 4;
@@ -576,6 +577,36 @@ __device__ __forceinline__ float l8_input(const char* s_in, const T* g_tile, int
   uint16_t h;
   asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(g_tile + j) : "memory");
   return __uint_as_float((uint32_t)h << 16);
+}
+
+// The lane's kmax (4, or 2 for flag lanes) input elements at tile element el,
+// widened to binary32, zeros past kv: one shared-memory vector load when the
+// whole piece is staged, element by element otherwise.
+template <typename T>
+__device__ __forceinline__ void l8_input_piece(const char* s_in, const T* g_tile, int el, int kv, int kmax,
+                                               int covered, float (&x)[4]) {
+  if (kv == kmax && el + kv <= covered) {
+    if constexpr (sizeof(T) == 4) {
+      if (kmax == 4) {
+        const float4 w = *reinterpret_cast<const float4*>(s_in + el * 4);
+        x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+      } else {
+        const float2 w = *reinterpret_cast<const float2*>(s_in + el * 4);
+        x[0] = w.x; x[1] = w.y; x[2] = 0.f; x[3] = 0.f;
+      }
+    } else {
+      if (kmax == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(s_in + el * 2);
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(s_in + el * 2);
+        x[0] = bf16lo(w); x[1] = bf16hi(w); x[2] = 0.f; x[3] = 0.f;
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; j++) x[j] = j < kv ? l8_input<T>(s_in, g_tile, el + j, covered) : 0.f;
 }
 
 // Check a group's flags as staged; re-poll stale lines from global memory.
@@ -618,15 +649,10 @@ __device__ __forceinline__ void l8_tile_same_layout(const RingArgs& a, const cha
         v[0] = __uint_as_float(rv.x); v[1] = __uint_as_float(rv.y);
         v[2] = __uint_as_float(rv.z); v[3] = __uint_as_float(rv.w);
       }
+      float x[4];
+      l8_input_piece<T>(s_in, g_in_tile, el, kv, kmax, covered, x);
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        if (j < kv) {
-          const float x = l8_input<T>(s_in, g_in_tile, el + j, covered);
-          v[j] = kRecvPartial ? __fadd_rn(v[j], x) : x;
-        } else {
-          v[j] = 0.f;
-        }
-      }
+      for (int j = 0; j < 4; j++) v[j] = j < kv ? (kRecvPartial ? __fadd_rn(v[j], x[j]) : x[j]) : 0.f;
       pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
     } else {
       pay = rv;  // final values pass through unchanged
@@ -663,10 +689,10 @@ __device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char
     const int el = (gl * 480 + L.piece_off) / 4;
     const int kv = (int)imax(0, imin(kmax, ne - el));
     const float p[4] = {__uint_as_float(rv.x), __uint_as_float(rv.y), __uint_as_float(rv.z), __uint_as_float(rv.w)};
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    float x[4], v[4];
+    l8_input_piece<uint16_t>(s_in, g_in_tile, el, kv, kmax, covered, x);
 #pragma unroll
-    for (int j = 0; j < 4; j++)
-      if (j < kv) v[j] = __fadd_rn(p[j], l8_input<uint16_t>(s_in, g_in_tile, el + j, covered));
+    for (int j = 0; j < 4; j++) v[j] = j < kv ? __fadd_rn(p[j], x[j]) : 0.f;
     const uint4 wv = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), 0u, 0u);  // rounded once
     if (kv > 0) store_out_n<uint16_t>(g_out_tile + el, kv, kmax, wv);
     for (int j = 0; j < kv; j++) fin[el + j] = (uint16_t)((j < 2 ? wv.x : wv.y) >> ((j & 1) * 16));
@@ -953,7 +979,7 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return e;
-  if (first_chunk >= kL8TileElems && grid <= sms) {
+  if (first_chunk >= kL8BulkMinChunk && grid <= sms) {
     const int nstages = f32 ? l8_max_stages<float>() : l8_max_stages<uint16_t>();
     const int smem = nstages * (f32 ? l8_stage_bytes<float>() : l8_stage_bytes<uint16_t>());
     static bool attr_set[2] = {false, false};
