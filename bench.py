@@ -201,6 +201,26 @@ def sweep(torch, B, steps, warmup, peak):
         ms = time_ring(c, torch, B, max(steps, 20), warmup)
         out[f"n4_{proto}_ch1_4KiB"] = {"stream_latency_us": round(statistics.median(ms) * 1e3, 2),
                                        "graph_latency_us": graph_latency_ring(c, torch, B)}
+    # busBW and roofline fraction vs size per protocol: N=8, seeded ring (seed
+    # 5), the sparse 8-channel mask 0b101101011011, f32, 1 KiB * 4^k per rank
+    # up to 1 GiB; small sizes timed from a CUDA graph (device time only)
+    sizes = {}
+    for proto in ("LL", "LL128", "Simple"):
+        row = {}
+        size = gen.KIB
+        while size <= (1 << 30):
+            c = gen.RingCase(f"sweep_{proto}_{size}", 8, gen.ring_permutation(8, 5), gen.SPARSE_MASK, proto,
+                             size // 4, gen.F32, "normal", 5, 0, 4)
+            if size <= 4 * gen.MIB:
+                t = graph_latency_ring(c, torch, B) / 1e6
+            else:
+                t = statistics.median(time_ring(c, torch, B, 3 if size >= 256 * gen.MIB else 5, 2)) / 1e3
+            row[f"{size // gen.KIB}KiB"] = {"busbw_gbs": round(busbw(c.bytes_per_rank, 8, t), 2),
+                                           "us": round(t * 1e6, 2),
+                                           "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
+            size *= 4
+        sizes[proto] = row
+    out["size_sweep_n8_sparse_mask_f32_default_buffers"] = sizes
     # one-shot bf16, N=8, 7168 x {1, 512}
     for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
         x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
@@ -271,39 +291,67 @@ def graph_latency_ring(case, torch, B):
 
 
 def e2e_ring(case, torch, B, steps, warmup):
-    """The same call measured end to end from pinned host buffers: every step
-    copies all ranks' inputs host->device, runs the AllReduce and copies every
-    rank's result back."""
+    """The same call measured end to end from pinned host buffers, through the
+    public API: every step copies all ranks' inputs host->device, runs the
+    AllReduce and copies every rank's output back device->host. Two device
+    buffer sets and three streams pipeline consecutive steps, so step k's
+    host->device copy overlaps step k-1's device->host copy (the two
+    directions of the host link run at once); the AllReduce calls stay ordered
+    on one stream and share one workspace."""
     x = device_inputs(case, torch)
     host_in = x.cpu().pin_memory()
-    host_out = torch.empty_like(host_in).pin_memory()
-    dx = torch.empty_like(x)
-    dy = torch.empty_like(x)
-    send = [dx[r] for r in range(case.nranks)]
-    recv = [dy[r] for r in range(case.nranks)]
+    host_out = [torch.empty_like(host_in).pin_memory() for _ in range(2)]
+    dx = [torch.empty_like(x) for _ in range(2)]
+    dy = [torch.empty_like(x) for _ in range(2)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
-    stream = torch.cuda.current_stream()
+    s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    h2d_done = [ev(), ev()]
+    cmp_done = [ev(), ev()]
+    d2h_done = [ev(), ev()]
+    for e in cmp_done + d2h_done:
+        e.record(torch.cuda.current_stream())
 
-    def one():
-        dx.copy_(host_in, non_blocking=True)
-        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
-        host_out.copy_(dy, non_blocking=True)
+    def one(k):
+        b = k % 2
+        s_h2d.wait_event(cmp_done[b])  # dx[b] no longer read by step k-2
+        with torch.cuda.stream(s_h2d):
+            dx[b].copy_(host_in, non_blocking=True)
+        h2d_done[b].record(s_h2d)
+        s_cmp.wait_event(h2d_done[b])
+        s_cmp.wait_event(d2h_done[b])  # dy[b] already copied out by step k-2
+        B.allreduce([dx[b][r] for r in range(case.nranks)], [dy[b][r] for r in range(case.nranks)], case.ring,
+                    case.mask, case.proto, ws, case.buff_size, case.chunk_steps, stream=s_cmp)
+        cmp_done[b].record(s_cmp)
+        s_d2h.wait_event(cmp_done[b])
+        with torch.cuda.stream(s_d2h):
+            host_out[b].copy_(dy[b], non_blocking=True)
+        d2h_done[b].record(s_d2h)
 
-    for _ in range(warmup):
-        one()
+    for k in range(warmup):
+        one(k)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
+    cur = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(cur)
+    for s_ in (s_h2d, s_cmp, s_d2h):
+        s_.wait_event(start)
+    for k in range(warmup, warmup + steps):
+        one(k)
+    for s_ in (s_h2d, s_cmp, s_d2h):
+        cur.wait_stream(s_)
+    end.record(cur)
     torch.cuda.synchronize()
     if B.get_status(ws) != B.Status.OK:
         raise RuntimeError("e2e: device status not OK")
-    t = a.elapsed_time(b) / 1e3 / steps
+    last = (warmup + steps - 1) % 2
+    if not torch.equal(host_out[last].view(torch.int32)[0], host_out[last].view(torch.int32)[1]):
+        raise RuntimeError("e2e: ranks 0 and 1 returned different results")
+    t = start.elapsed_time(end) / 1e3 / steps
     nbytes = case.nranks * case.bytes_per_rank
     return {"value": round(busbw(case.bytes_per_rank, case.nranks, t), 2), "unit": UNIT,
-            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": round(t * 1e3, 3)}
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "ms_per_step": round(t * 1e3, 3),
+            "pipelining": "2 buffer sets; step k host->device overlaps step k-1 device->host"}
 
 
 def cpu_baseline(case, budget_s=10.0):
@@ -328,6 +376,20 @@ def cpu_baseline(case, budget_s=10.0):
             "sample": f"the whole headline call (8 ranks x 64 MiB f32) through the oracle's step-by-step "
                       f"simulation, best of {len(times)}, 1 thread; host has {os.cpu_count()} cores",
             "seconds_per_call": round(t, 3)}
+
+
+def combine_replicas(total_ms, steps, bytes_per_rank, nranks, world, dist=None, device="cpu"):
+    """Whole-job figures over `world` independent replicas (one per GPU): the
+    time is the slowest replica's (max over ranks); the throughput is the
+    bytes of all replicas over that time, as busBW. Returns (ms_per_step,
+    value)."""
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / steps
+    return ms_per_step, busbw(bytes_per_rank, nranks, ms_per_step / 1e3) * world
 
 
 def run_gpu(args):
@@ -378,12 +440,8 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st.name}")
     total_ms = start.elapsed_time(end)
     launch_ms = [a.elapsed_time(b) for a, b in per]
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = busbw(case.bytes_per_rank, case.nranks, ms_per_step / 1e3) * world
+    ms_per_step, value = combine_replicas(total_ms, args.steps, case.bytes_per_rank, case.nranks, world,
+                                          dist if world > 1 else None, "cuda")
     avg_launch = statistics.mean(launch_ms) / 1e3
     algo = algorithmic_bytes(case)
     achieved = algo / avg_launch / 1e9

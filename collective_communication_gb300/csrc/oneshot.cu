@@ -65,6 +65,11 @@ __device__ __forceinline__ void os_store_scalar<uint16_t>(uint16_t* p, float v) 
   *p = *reinterpret_cast<uint16_t*>(&b);
 }
 
+// Peers are read in batches of kBatch ranks: every load of a batch is issued
+// before any is added, so a thread keeps kBatch x U 16-byte loads in flight;
+// the additions then run strictly in rank order.
+constexpr int kBatch = 8;
+
 template <typename T>
 __global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_constant__ OneShotArgs a) {
   constexpr int P = OsPack<T>::kElems;
@@ -78,30 +83,37 @@ __global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_c
   const int64_t per_tile = (int64_t)kOneShotThreads * U;
   for (int64_t base = tile * per_tile; base < npack; base += ntiles * per_tile) {
     float acc[U][8];
-    uint4 w[U];
+    for (int q0 = 0; q0 < N; q0 += kBatch) {
+      uint4 w[kBatch][U];
 #pragma unroll
-    for (int u = 0; u < U; u++) {
-      const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-      if (p < npack) {
-        w[u] = ld_stream_v4(reinterpret_cast<const T*>(a.send[0]) + p * P);
-        OsPack<T>::widen(w[u], acc[u]);
-      }
-    }
-    for (int q = 1; q < N; q++) {
-      const T* src = reinterpret_cast<const T*>(a.send[q]);
+      for (int b = 0; b < kBatch; b++) {
+        if (q0 + b < N) {
+          const T* src = reinterpret_cast<const T*>(a.send[q0 + b]);
 #pragma unroll
-      for (int u = 0; u < U; u++) {
-        const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-        if (p < npack) w[u] = ld_stream_v4(src + p * P);
+          for (int u = 0; u < U; u++) {
+            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+            if (p < npack) w[b][u] = ld_stream_v4(src + p * P);
+          }
+        }
       }
 #pragma unroll
-      for (int u = 0; u < U; u++) {
-        const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-        if (p < npack) {
-          float v[8];
-          OsPack<T>::widen(w[u], v);
+      for (int b = 0; b < kBatch; b++) {
+        if (q0 + b < N) {
 #pragma unroll
-          for (int j = 0; j < P; j++) acc[u][j] = __fadd_rn(acc[u][j], v[j]);
+          for (int u = 0; u < U; u++) {
+            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+            if (p < npack) {
+              float v[8];
+              OsPack<T>::widen(w[b][u], v);
+              if (q0 + b == 0) {
+#pragma unroll
+                for (int j = 0; j < P; j++) acc[u][j] = v[j];  // the sum starts at x_0
+              } else {
+#pragma unroll
+                for (int j = 0; j < P; j++) acc[u][j] = __fadd_rn(acc[u][j], v[j]);
+              }
+            }
+          }
         }
       }
     }

@@ -214,6 +214,13 @@ __device__ __forceinline__ void tma_load_1d(void* smem_dst, const void* gmem_src
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+// Store with an L2 eviction policy (user output: evict-first, so that the
+// streaming output does not push FIFO lines out of L2).
+__device__ __forceinline__ void st_v4_policy(void* p, uint4 v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
+               : "memory");
+}
 // Orders this thread's earlier generic-proxy accesses (here: the acquire of a
 // FIFO tail) before its later async-proxy (bulk copy) accesses of global memory.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }

@@ -953,8 +953,11 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
 }
 
 cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
-  constexpr int kThreadsLL = 1024;     // one line unit per thread, many warps
-  constexpr int kThreadsLL128 = 1024;  // one 4-line group per warp pass, many warps
+  // Polling forms: 256 threads when a step is a few passes of the block at
+  // most (fewer threads per barrier: lower latency), 1024 threads for large
+  // LL steps (more warps in flight).
+  constexpr int kThreadsSmall = 256;
+  constexpr int kThreadsLarge = 1024;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -965,15 +968,23 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool f32 = a.geo.dtype == kF32;
+  const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
   if (a.geo.proto == kLL) {
-    cfg.blockDim = dim3(kThreadsLL);
-    if (threads_out) *threads_out = kThreadsLL;
-    return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLL>, a)
-               : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLL>, a);
+    const bool small = div_up(first_chunk, f32 ? LLUnit<float>::kElems : LLUnit<uint16_t>::kElems) <=
+                       8 * kThreadsSmall;
+    if (small) {
+      cfg.blockDim = dim3(kThreadsSmall);
+      if (threads_out) *threads_out = kThreadsSmall;
+      return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsSmall>, a)
+                 : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsSmall>, a);
+    }
+    cfg.blockDim = dim3(kThreadsLarge);
+    if (threads_out) *threads_out = kThreadsLarge;
+    return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLarge>, a)
+               : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLarge>, a);
   }
   // LL128: the bulk form once the first loop's chunks span a whole tile,
   // the polling form (lowest latency) for smaller messages.
-  const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
   int device = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -996,10 +1007,10 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
     return f32 ? cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<float>, a, nstages)
                : cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<uint16_t>, a, nstages);
   }
-  cfg.blockDim = dim3(kThreadsLL128);
-  if (threads_out) *threads_out = kThreadsLL128;
-  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsLL128>, a)
-             : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL128, kThreadsLL128>, a);
+  cfg.blockDim = dim3(kThreadsSmall);
+  if (threads_out) *threads_out = kThreadsSmall;
+  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsSmall>, a)
+             : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL128, kThreadsSmall>, a);
 }
 
 }  // namespace rar

@@ -142,7 +142,7 @@ __device__ __forceinline__ uint16_t load_final_scalar<uint16_t>(const char* p) {
 template <typename T, int PRIM>
 __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv, const T* __restrict__ g_in,
                                              T* __restrict__ g_out, const char* rslot, char* sslot, int64_t e0,
-                                             int ne, int covered, int ct, int nct) {
+                                             int ne, int covered, int ct, int nct, uint64_t out_policy) {
   constexpr int P = ElemTraits<T>::kPack;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
@@ -186,7 +186,7 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
         if (PRIM == kRecvReduceCopySend) fin = to_final_pack<T>(v);
         if (kSendPartial) store_partial_pack<P>(sslot + e * 4, v);
         if (kSendFinal) st_v4(sslot + e * (int64_t)sizeof(T), fin);
-        if (kOut) st_v4(g_out + e, fin);
+        if (kOut) st_v4_policy(g_out + e, fin, out_policy);  // streamed out: evict-first in L2
       }
     }
   }
@@ -213,19 +213,19 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
 template <typename T>
 __device__ __forceinline__ void tile_compute_any(int prim, const char* s_in, const char* s_rcv, const T* g_in,
                                                  T* g_out, const char* rslot, char* sslot, int64_t e0, int ne,
-                                                 int covered, int ct, int nct) {
+                                                 int covered, int ct, int nct, uint64_t pol) {
   switch (prim) {
-    case kSend: tile_compute<T, kSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct); break;
+    case kSend: tile_compute<T, kSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol); break;
     case kRecvReduceSend:
-      tile_compute<T, kRecvReduceSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      tile_compute<T, kRecvReduceSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
       break;
     case kRecvReduceCopySend:
-      tile_compute<T, kRecvReduceCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      tile_compute<T, kRecvReduceCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
       break;
     case kRecvCopySend:
-      tile_compute<T, kRecvCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct);
+      tile_compute<T, kRecvCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
       break;
-    default: tile_compute<T, kRecv>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct); break;
+    default: tile_compute<T, kRecv>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol); break;
   }
 }
 
@@ -409,6 +409,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   } else {
     // ---- workers ----
     const int ct = threadIdx.x - 96;
+    const uint64_t out_pol = l2_policy_evict_first();
     uint64_t rstep = base_recv, sstep = base_send;
     uint32_t gt = 0;
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         const char* s_in = smem + (int64_t)st * SB;
         const char* s_rcv = s_in + kTileElems * (int)sizeof(T);
         tile_compute_any<T>(c.prim, s_in, s_rcv, in + c.offset, out + c.offset, rslot, sslot, e0, ne, ne / P * P,
-                            ct, kComputeThreads);
+                            ct, kComputeThreads, out_pol);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);
       }
