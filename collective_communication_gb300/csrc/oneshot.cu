@@ -136,7 +136,6 @@ __global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_c
 cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
   const int P = a.dtype == kF32 ? 4 : 8;
   const int64_t npack = a.count / P;
-  const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -147,15 +146,16 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (device < 64) sm_count[device] = sms;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;
   // enough tiles to fill every SM several times over, never more than needed
   int64_t tiles = div_up(npack, per_tile);
   const int64_t cap = div_up((int64_t)sms * 8, a.nranks);
   if (tiles > cap) tiles = cap;
   if (tiles < 1) tiles = 1;
-  cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(tiles * a.nranks));
   cfg.blockDim = dim3(kOneShotThreads);
-  cfg.stream = stream;
   if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_kernel<float>, a);
   return cudaLaunchKernelEx(&cfg, oneshot_kernel<uint16_t>, a);
 }

@@ -147,7 +147,8 @@ RAR_API rar_status rar_allreduce(const void* const* sendbufs, void* const* recvb
  *   (the ranks read each other's inputs while writing their outputs) nor
  *   another receive buffer, else RAR_ERR_ARG.
  * dtype: RAR_BF16 or RAR_F32; op: RAR_SUM; count 0 returns RAR_OK.
- * Needs no workspace. Errors: RAR_ERR_ARG, RAR_ERR_ALIGN, RAR_ERR_CUDA.
+ * Needs no workspace and waits on nothing. Errors: RAR_ERR_ARG,
+ * RAR_ERR_ALIGN, RAR_ERR_CUDA.
  */
 RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbufs, int nranks,
                        size_t count, rar_dtype dtype, rar_redop op, void* stream);

@@ -51,3 +51,10 @@ def test_oneshot_ragged(n, count, dtype):
 
 def test_oneshot_integer_exact():
     run_oneshot(8, 50000, "bf16", "int8", 3)
+
+
+@pytest.mark.parametrize("n", [2, 5, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_oneshot_many_tiles(n, dtype):
+    """Many grid-stride passes and a ragged end."""
+    run_oneshot(n, 8192 * 40 + 4096 + 24 + 3, dtype, "normal", 40 + n)
