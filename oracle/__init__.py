@@ -64,9 +64,9 @@ def lib():
         L.orc_ll128_encode.argtypes = [P, SZ, U64, P]
         L.orc_ll128_decode.argtypes = [P, SZ, U64, P]
         L.orc_ll128_decode.restype = SZ
-        L.orc_ring_allreduce_sim.argtypes = [P, P, I, SZ, I, P, U64, I, SZ, I, P, P, P]
-        L.orc_ring_allreduce_closed.argtypes = [P, P, I, SZ, I, P, U64, I, SZ, I]
-        L.orc_ring_closed_at.argtypes = [P, I, SZ, I, P, U64, I, SZ, I, P, SZ, P, P]
+        L.orc_ring_allreduce_sim.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I, I, P, P, P]
+        L.orc_ring_allreduce_closed.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I]
+        L.orc_ring_closed_at.argtypes = [P, I, SZ, I, P, I, U64, I, SZ, I, P, SZ, P, P]
         L.orc_oneshot.argtypes = [P, P, I, SZ, I]
         L.orc_state_model.argtypes = [I, I, I, I, P]
         L.orc_bf16_round.argtypes = [P, P, SZ]
@@ -80,6 +80,15 @@ def _ptr(a):
 
 def _i32(seq):
     return np.ascontiguousarray(np.asarray(seq, dtype=np.int32))
+
+
+def _rings(ring_order):
+    """One ring (a list of ranks) or one ring per dense channel (a list of
+    lists) -> (flat int32 array, number of rings)."""
+    a = np.asarray(ring_order, dtype=np.int32)
+    if a.ndim == 1:
+        return np.ascontiguousarray(a), 1
+    return np.ascontiguousarray(a.reshape(-1)), a.shape[0]
 
 
 def _check(code, what):
@@ -201,10 +210,13 @@ def _prep(inputs):
     return ins, dt
 
 
-def ring_allreduce_sim(inputs, ring_order, mask, proto, buff_size=0, chunk_steps=4, outputs=None):
+def ring_allreduce_sim(inputs, ring_order, mask, proto, buff_size=0, chunk_steps=4, outputs=None,
+                       direct=False):
     """Step-by-step simulation. Returns (outputs, sends, recvs, loops per channel).
 
-    `outputs` may be given (e.g. the inputs themselves, for an in-place call)."""
+    ring_order: one ring, or one ring per dense channel. `outputs` may be given
+    (e.g. the inputs themselves, for an in-place call). direct: Simple only,
+    all-gather hops write the next rank's output instead of a FIFO slot."""
     ins, dt = _prep(inputs)
     n = len(ins)
     count = ins[0].size
@@ -212,8 +224,9 @@ def ring_allreduce_sim(inputs, ring_order, mask, proto, buff_size=0, chunk_steps
     sends = np.zeros(n, np.int64)
     recvs = np.zeros(n, np.int64)
     loops = np.zeros(64, np.int64)
-    st = lib().orc_ring_allreduce_sim(_ptr_array(ins), _ptr_array(outs), n, count, dt,
-                                      _ptr(_i32(ring_order)), mask, proto, buff_size, chunk_steps,
+    rings, nrings = _rings(ring_order)
+    st = lib().orc_ring_allreduce_sim(_ptr_array(ins), _ptr_array(outs), n, count, dt, _ptr(rings), nrings,
+                                      mask, proto, buff_size, chunk_steps, int(direct),
                                       _ptr(sends), _ptr(recvs), _ptr(loops))
     _check(st, "ring_allreduce_sim")
     return outs, sends, recvs, loops[:len(mask_channels(mask))]
@@ -223,8 +236,9 @@ def ring_allreduce_closed(inputs, ring_order, mask, proto, buff_size=0, chunk_st
     ins, dt = _prep(inputs)
     n = len(ins)
     outs = [np.zeros_like(a) for a in ins]
+    rings, nrings = _rings(ring_order)
     st = lib().orc_ring_allreduce_closed(_ptr_array(ins), _ptr_array(outs), n, ins[0].size, dt,
-                                         _ptr(_i32(ring_order)), mask, proto, buff_size, chunk_steps)
+                                         _ptr(rings), nrings, mask, proto, buff_size, chunk_steps)
     _check(st, "ring_allreduce_closed")
     return outs
 
@@ -241,7 +255,8 @@ def ring_closed_at(sampled, ring_order, mask, proto, idx, count, buff_size=0, ch
         raise ValueError("one sampled value per index and rank")
     out = np.zeros(m, ins[0].dtype)
     chunks = np.zeros(m, np.int32)
-    st = lib().orc_ring_closed_at(_ptr_array(ins), n, count, dt, _ptr(_i32(ring_order)), mask,
+    rings, nrings = _rings(ring_order)
+    st = lib().orc_ring_closed_at(_ptr_array(ins), n, count, dt, _ptr(rings), nrings, mask,
                                   proto, buff_size, chunk_steps, _ptr(idx), m, _ptr(out),
                                   _ptr(chunks))
     _check(st, "ring_closed_at")

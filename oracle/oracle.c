@@ -472,6 +472,7 @@ typedef struct {
   uint8_t* pay_in;          /* scratch payload */
   uint8_t* pay_out;
   float* vals;              /* scratch binary32 values */
+  int direct;               /* Simple only: all-gather hops write the next rank's output */
 } sim_t;
 
 /* One slice of one rank's program. */
@@ -572,8 +573,20 @@ static int sim_try_slice(sim_t* S, int i, const slice_t* sl) {
   int e_send = i, e_recv = (i - 1 + n) % n;
   int prim = sl->prim;
   size_t nelem = sl->nelem;
-  if (has_send(prim) && !fifo_can_send(S, e_send, S->sstep[i])) return 0;
-  if (has_recv(prim)) {
+  /* Direct all-gather ([C23] "发布顺序与 Fence", direct read/write; [C12]
+   * "源码步骤三" .. "源码步骤五"): a hop that carries a final value writes it
+   * straight into the next rank's output at the same offset instead of a FIFO
+   * slot, then publishes the tail as usual; its receiver waits for the tail and
+   * finds the value already in its own output. No slot is filled, so the
+   * sender skips the credit wait; the step counters advance as before. */
+  int direct_send = S->direct && (prim == ORC_RECV_REDUCE_COPY_SEND || prim == ORC_RECV_COPY_SEND);
+  int direct_recv = S->direct && (prim == ORC_RECV_COPY_SEND || prim == ORC_RECV);
+  int r_next = S->rank_at[(i + 1) % n];
+  if (has_send(prim) && !direct_send && !fifo_can_send(S, e_send, S->sstep[i])) return 0;
+  if (direct_recv) {
+    if (S->conn[e_recv].tail < S->rstep[i] + (uint64_t)g->sps) return 0;
+    for (size_t j = 0; j < nelem; j++) S->vals[j] = load_as_f32(S->recv[r], g->dtype, sl->offset + j);
+  } else if (has_recv(prim)) {
     size_t nb = payload_bytes(g, recvs_partial(prim), nelem);
     if (!fifo_try_recv(S, e_recv, S->rstep[i], nb)) return 0;
     unpack_values(g, recvs_partial(prim), S->pay_in, nelem, S->vals);
@@ -597,15 +610,20 @@ static int sim_try_slice(sim_t* S, int i, const slice_t* sl) {
       }
       case ORC_RECV_COPY_SEND:
       case ORC_RECV:
-        store_from_f32(S->recv[r], g->dtype, el, S->vals[j]);
+        if (!direct_recv) store_from_f32(S->recv[r], g->dtype, el, S->vals[j]);
         break;
     }
   }
   if (has_send(prim)) {
-    size_t nb = payload_bytes(g, sends_partial(prim), nelem);
-    pack_values(g, sends_partial(prim), S->vals, nelem, S->pay_out);
-    int st = fifo_send(S, e_send, S->sstep[i], nb);
-    if (st != ORC_OK) return -st;
+    if (direct_send) {
+      for (size_t j = 0; j < nelem; j++) store_from_f32(S->recv[r_next], g->dtype, sl->offset + j, S->vals[j]);
+      S->conn[e_send].tail = S->sstep[i] + (uint64_t)g->sps; /* data first, then the tail */
+    } else {
+      size_t nb = payload_bytes(g, sends_partial(prim), nelem);
+      pack_values(g, sends_partial(prim), S->vals, nelem, S->pay_out);
+      int st = fifo_send(S, e_send, S->sstep[i], nb);
+      if (st != ORC_OK) return -st;
+    }
     S->sstep[i] += (uint64_t)g->sps;
     S->sends[r]++;
   }
@@ -614,9 +632,11 @@ static int sim_try_slice(sim_t* S, int i, const slice_t* sl) {
     S->conn[e_recv].head = S->rstep[i]; /* release the slots just read */
     S->recvs[r]++;
   }
-  /* credit bound: never more than NCCL_STEPS steps outstanding on an edge */
-  for (int e = 0; e < n; e++)
-    if (S->conn[e].tail > S->conn[e].head + NSTEPS) return -ORC_ECHECK;
+  /* credit bound: never more than NCCL_STEPS steps outstanding on an edge
+   * (direct all-gather steps occupy no slot, so the bound holds for FIFO use only) */
+  if (!S->direct)
+    for (int e = 0; e < n; e++)
+      if (S->conn[e].tail > S->conn[e].head + NSTEPS) return -ORC_ECHECK;
   return 1;
 }
 
@@ -658,15 +678,19 @@ static size_t build_program(const geom_t* g, int i, size_t gridOffset, size_t ch
  * ORC_EDEADLOCK.
  */
 int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nranks, size_t count,
-                           int dtype, const int* ring_order, uint64_t mask, int proto,
-                           size_t buffSize, int chunkSteps, int64_t* sends, int64_t* recvs,
+                           int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
+                           size_t buffSize, int chunkSteps, int direct, int64_t* sends, int64_t* recvs,
                            int64_t* loops_out) {
   geom_t g;
   int st = geom_init(&g, proto, dtype, nranks, mask, count, buffSize, chunkSteps);
   if (st != ORC_OK) return st;
+  if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
+  if (direct && proto != ORC_SIMPLE) return ORC_EARG;
   int rank_at[MAXR];
-  st = rank_at_index(nranks, ring_order, rank_at);
-  if (st != ORC_OK) return st;
+  for (int ch = 0; ch < nrings; ch++) {
+    st = rank_at_index(nranks, ring_order + (size_t)ch * nranks, rank_at);
+    if (st != ORC_OK) return st;
+  }
   int64_t dummy_s[MAXR] = {0}, dummy_r[MAXR] = {0};
   if (!sends) sends = dummy_s;
   if (!recvs) recvs = dummy_r;
@@ -695,8 +719,11 @@ int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nrank
   S.pay_in = pin;
   S.pay_out = pout;
   S.vals = vals;
+  S.direct = direct;
 
   for (int ch = 0; ch < g.nchan; ch++) {
+    /* this channel's ring ([C12] "GRAPH 重建：N=4": channels may use different ring orders) */
+    rank_at_index(nranks, ring_order + (nrings == 1 ? 0 : (size_t)ch * nranks), rank_at);
     size_t gridOffset, channelCount;
     channel_range(&g, ch, &gridOffset, &channelCount);
     /* a fresh connector set per channel: FIFOs zeroed, steps from 0 */
@@ -773,16 +800,17 @@ static float ring_fold(const geom_t* g, const void* const* send, const int* rank
 }
 
 int orc_ring_allreduce_closed(const void* const* send, void* const* recv, int nranks, size_t count,
-                              int dtype, const int* ring_order, uint64_t mask, int proto,
+                              int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
                               size_t buffSize, int chunkSteps) {
   geom_t g;
   int st = geom_init(&g, proto, dtype, nranks, mask, count, buffSize, chunkSteps);
   if (st != ORC_OK) return st;
+  if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
   int rank_at[MAXR];
-  st = rank_at_index(nranks, ring_order, rank_at);
-  if (st != ORC_OK) return st;
   size_t loopCount = (size_t)nranks * g.chunk_elems;
   for (int ch = 0; ch < g.nchan; ch++) {
+    st = rank_at_index(nranks, ring_order + (nrings == 1 ? 0 : (size_t)ch * nranks), rank_at);
+    if (st != ORC_OK) return st;
     size_t gridOffset, channelCount;
     channel_range(&g, ch, &gridOffset, &channelCount);
     for (size_t elemOffset = 0; elemOffset < channelCount; elemOffset += loopCount) {
@@ -809,20 +837,21 @@ int orc_ring_allreduce_closed(const void* const* send, void* const* recv, int nr
  * chunk_out[k] (optional) = the chunk index c that element idx[k] lies in.
  */
 int orc_ring_closed_at(const void* const* sampled, int nranks, size_t count, int dtype,
-                       const int* ring_order, uint64_t mask, int proto, size_t buffSize,
+                       const int* ring_order, int nrings, uint64_t mask, int proto, size_t buffSize,
                        int chunkSteps, const int64_t* idx, size_t m, void* out,
                        int32_t* chunk_out) {
   geom_t g;
   int st = geom_init(&g, proto, dtype, nranks, mask, count, buffSize, chunkSteps);
   if (st != ORC_OK) return st;
+  if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
   int rank_at[MAXR];
-  st = rank_at_index(nranks, ring_order, rank_at);
-  if (st != ORC_OK) return st;
   size_t loopCount = (size_t)nranks * g.chunk_elems;
   for (size_t k = 0; k < m; k++) {
     if (idx[k] < 0 || (size_t)idx[k] >= count) return ORC_EARG;
     size_t el = (size_t)idx[k];
     int ch = (int)(el / g.per_channel);
+    st = rank_at_index(nranks, ring_order + (nrings == 1 ? 0 : (size_t)ch * nranks), rank_at);
+    if (st != ORC_OK) return st;
     size_t gridOffset, channelCount;
     channel_range(&g, ch, &gridOffset, &channelCount);
     size_t off = el - gridOffset;
