@@ -139,21 +139,31 @@ rar_status rar_workspace_init(void* workspace, size_t workspaceBytes, int nranks
   return from_cuda(cudaGetLastError());
 }
 
-rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
-                         rar_dtype dtype, rar_redop op, const int* ring_order, uint64_t channelMask,
-                         rar_proto proto, size_t buffSize, int chunkSteps, void* workspace, size_t workspaceBytes,
-                         void* stream) {
+rar_status rar_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                            rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
+                            rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, void* workspace,
+                            size_t workspaceBytes, void* stream) {
   if (op != RAR_SUM) return RAR_ERR_ARG;
   if (count > (size_t)INT64_MAX / 4) return RAR_ERR_ARG;
+  if ((flags & ~(unsigned)RAR_FLAG_DIRECT) != 0) return RAR_ERR_ARG;
+  const bool direct = (flags & RAR_FLAG_DIRECT) != 0;
+  if (direct && proto != RAR_SIMPLE) return RAR_ERR_ARG;
   Geometry g;
   if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
                     chunkSteps) != 0)
     return RAR_ERR_ARG;
+  if (nrings != 1 && nrings != g.nchan) return RAR_ERR_ARG;
+  if (ring_orders == nullptr) return RAR_ERR_ARG;
   RingArgs a;
   std::memset(&a, 0, sizeof a);
-  rar_status st = setup_ring(nranks, ring_order, a.ring_index);
-  if (st != RAR_OK) return st;
-  st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * g.elem_bytes, true);
+  // one ring for every channel, or one per dense channel ([C12] "GRAPH 重建：N=4")
+  for (int ch = 0; ch < g.nchan; ch++) {
+    int idx[kMaxRanks];
+    const rar_status st = setup_ring(nranks, ring_orders + (nrings == 1 ? 0 : (size_t)ch * nranks), idx);
+    if (st != RAR_OK) return st;
+    for (int r = 0; r < nranks; r++) a.ring_index[ch * kMaxRanks + r] = (uint8_t)idx[r];
+  }
+  rar_status st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * g.elem_bytes, true);
   if (st != RAR_OK) return st;
   if (workspace == nullptr) return RAR_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
@@ -172,10 +182,19 @@ rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int
   a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
   a.timeout_ns = spin_timeout_ns();
   a.fault = g_fault.load(std::memory_order_relaxed);
+  a.direct = direct ? 1 : 0;
   const int grid = nranks * g.nchan;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = (g.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr) : launch_ring_line(a, grid, s, nullptr);
   return from_cuda(e);
+}
+
+rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                         rar_dtype dtype, rar_redop op, const int* ring_order, uint64_t channelMask,
+                         rar_proto proto, size_t buffSize, int chunkSteps, void* workspace, size_t workspaceBytes,
+                         void* stream) {
+  return rar_allreduce_ex(sendbufs, recvbufs, nranks, count, dtype, op, ring_order, 1, channelMask, proto, buffSize,
+                          chunkSteps, 0u, workspace, workspaceBytes, stream);
 }
 
 rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,

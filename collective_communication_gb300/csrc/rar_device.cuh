@@ -72,7 +72,8 @@ constexpr int kFaultDropHead = 1;   // receivers never publish their head
 struct RingArgs {
   const void* send[kMaxRanks];
   void* recv[kMaxRanks];
-  int ring_index[kMaxRanks];  // ring index of user rank r
+  uint8_t ring_index[kMaxChannels * kMaxRanks];  // [dense channel * kMaxRanks + user rank] -> ring index
+  int direct;                  // Simple: all-gather hops write the next rank's output directly
   Geometry geo;
   uint64_t mask;
   char* ws;                    // workspace base
@@ -292,6 +293,18 @@ __device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* den
     uint64_t below = tid == 0 ? 0ull : (a.mask & ((1ull << tid) - 1ull));
     if (__popcll(below) == *dense) *sh_chan_id = tid;
   }
+}
+
+// Ring index of user rank `rank` on dense channel `dense`, and the user rank
+// that follows it on that channel's ring.
+__device__ __forceinline__ int ring_index_of(const RingArgs& a, int dense, int rank) {
+  return a.ring_index[dense * kMaxRanks + rank];
+}
+__device__ __forceinline__ int next_rank_of(const RingArgs& a, int dense, int ring_idx) {
+  const int want = (ring_idx + 1) % a.geo.nranks;
+  for (int r = 0; r < a.geo.nranks; r++)
+    if (a.ring_index[dense * kMaxRanks + r] == want) return r;
+  return 0;
 }
 
 // Entry check shared by the ring kernels (thread 0): the workspace must be

@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   map_block(a, &rank, &dense, &sh_chan);
   __syncthreads();
   const int N = g.nranks;
-  const int ring_idx = a.ring_index[rank];
+  const int ring_idx = ring_index_of(a, dense, rank);
   const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
   ConnCounters* cs = conn_at(a, dense, e_send);
   ConnCounters* cr = conn_at(a, dense, e_recv);
@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
   map_block(a, &rank, &dense, &sh_chan);
   __syncthreads();
   const int N = g.nranks;
-  const int ring_idx = a.ring_index[rank];
+  const int ring_idx = ring_index_of(a, dense, rank);
   const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
   ConnCounters* cs = conn_at(a, dense, e_send);
   ConnCounters* cr = conn_at(a, dense, e_recv);

@@ -139,17 +139,24 @@ __device__ __forceinline__ uint16_t load_final_scalar<uint16_t>(const char* p) {
 // memory (the pack-aligned prefix of `covered` elements); g_in / g_out: user
 // buffers at the slice's first element; rslot / sslot: the slice's FIFO bytes
 // on the receive / send connection; e0: the tile's first element in the slice.
-template <typename T, int PRIM>
+// DIRECT (all-gather hops of the direct mode): final values go straight to
+// the next rank's output (g_next) instead of the send FIFO, and a received
+// final is already in this rank's own output (staged from there, not from the
+// FIFO), so it is neither stored again nor, on the last row, moved at all.
+template <typename T, int PRIM, bool DIRECT>
 __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv, const T* __restrict__ g_in,
-                                             T* __restrict__ g_out, const char* rslot, char* sslot, int64_t e0,
-                                             int ne, int covered, int ct, int nct, uint64_t out_policy) {
+                                             T* __restrict__ g_out, T* __restrict__ g_next, const char* rslot,
+                                             char* sslot, int64_t e0, int ne, int covered, int ct, int nct,
+                                             uint64_t out_policy) {
   constexpr int P = ElemTraits<T>::kPack;
   constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
   constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecvFinal = PRIM == kRecvCopySend || PRIM == kRecv;
+  constexpr bool kRecvFinal = (PRIM == kRecvCopySend || PRIM == kRecv) && !(DIRECT && PRIM == kRecv);
   constexpr bool kSendPartial = PRIM == kSend || PRIM == kRecvReduceSend;
-  constexpr bool kSendFinal = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend;
-  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
+  constexpr bool kSendFinal = (PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend) && !DIRECT;
+  constexpr bool kSendNext = (PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend) && DIRECT;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || ((PRIM == kRecvCopySend || PRIM == kRecv) && !DIRECT);
+  if constexpr (DIRECT && PRIM == kRecv) return;  // the data is already in place
   constexpr int U = 4;
   const int npacks = covered / P;
   for (int j0 = ct; j0 < npacks; j0 += nct * U) {
@@ -186,6 +193,7 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
         if (PRIM == kRecvReduceCopySend) fin = to_final_pack<T>(v);
         if (kSendPartial) store_partial_pack<P>(sslot + e * 4, v);
         if (kSendFinal) st_v4(sslot + e * (int64_t)sizeof(T), fin);
+        if (kSendNext) st_v4(g_next + e, fin);  // read back by the next rank: default L2 policy
         if (kOut) st_v4_policy(g_out + e, fin, out_policy);  // streamed out: evict-first in L2
       }
     }
@@ -197,7 +205,9 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
     T fv{};
     if (kIn) xv = load_input_scalar<T>(g_in + e);
     if (kRecvPartial) pv = __uint_as_float(ld_cg_u32(rslot + e * 4));
-    if (kRecvFinal) fv = load_final_scalar<T>(rslot + e * (int64_t)sizeof(T));
+    if (kRecvFinal)
+      fv = DIRECT ? load_final_scalar<T>(reinterpret_cast<const char*>(g_out + e))
+                  : load_final_scalar<T>(rslot + e * (int64_t)sizeof(T));
     if (PRIM == kSend) {
       *reinterpret_cast<float*>(sslot + e * 4) = xv;
     } else if (PRIM == kRecvReduceSend) {
@@ -207,26 +217,53 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
     }
     if (kOut) g_out[e] = fv;
     if (kSendFinal) *reinterpret_cast<T*>(sslot + e * (int64_t)sizeof(T)) = fv;
+    if (kSendNext) g_next[e] = fv;
+  }
+}
+
+template <typename T, bool DIRECT>
+__device__ __forceinline__ void tile_compute_prim(int prim, const char* s_in, const char* s_rcv, const T* g_in,
+                                                  T* g_out, T* g_next, const char* rslot, char* sslot, int64_t e0,
+                                                  int ne, int covered, int ct, int nct, uint64_t pol) {
+  switch (prim) {
+    case kSend:
+      tile_compute<T, kSend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct, pol);
+      break;
+    case kRecvReduceSend:
+      tile_compute<T, kRecvReduceSend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct,
+                                               nct, pol);
+      break;
+    case kRecvReduceCopySend:
+      tile_compute<T, kRecvReduceCopySend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered,
+                                                   ct, nct, pol);
+      break;
+    case kRecvCopySend:
+      tile_compute<T, kRecvCopySend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct,
+                                             nct, pol);
+      break;
+    default:
+      tile_compute<T, kRecv, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct, pol);
+      break;
   }
 }
 
 template <typename T>
-__device__ __forceinline__ void tile_compute_any(int prim, const char* s_in, const char* s_rcv, const T* g_in,
-                                                 T* g_out, const char* rslot, char* sslot, int64_t e0, int ne,
-                                                 int covered, int ct, int nct, uint64_t pol) {
-  switch (prim) {
-    case kSend: tile_compute<T, kSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol); break;
-    case kRecvReduceSend:
-      tile_compute<T, kRecvReduceSend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
-      break;
-    case kRecvReduceCopySend:
-      tile_compute<T, kRecvReduceCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
-      break;
-    case kRecvCopySend:
-      tile_compute<T, kRecvCopySend>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol);
-      break;
-    default: tile_compute<T, kRecv>(s_in, s_rcv, g_in, g_out, rslot, sslot, e0, ne, covered, ct, nct, pol); break;
-  }
+__device__ __forceinline__ void tile_compute_any(bool direct, int prim, const char* s_in, const char* s_rcv,
+                                                 const T* g_in, T* g_out, T* g_next, const char* rslot, char* sslot,
+                                                 int64_t e0, int ne, int covered, int ct, int nct, uint64_t pol) {
+  if (direct)
+    tile_compute_prim<T, true>(prim, s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct, pol);
+  else
+    tile_compute_prim<T, false>(prim, s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct, pol);
+}
+
+// Rows of the direct mode: all-gather sends go to the next rank's output,
+// all-gather receives find their data in this rank's own output.
+__device__ __forceinline__ bool direct_send_row(bool direct, int prim) {
+  return direct && (prim == kRecvReduceCopySend || prim == kRecvCopySend);
+}
+__device__ __forceinline__ bool direct_recv_row(bool direct, int prim) {
+  return direct && (prim == kRecvCopySend || prim == kRecv);
 }
 
 constexpr int kTileElems = 8192;    // elements per bulk-copied tile
@@ -264,7 +301,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   map_block(a, &rank, &dense, &sh_chan);
   __syncthreads();
   const int N = g.nranks;
-  const int ring_idx = a.ring_index[rank];
+  const int ring_idx = ring_index_of(a, dense, rank);
   const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
   ConnCounters* cs = conn_at(a, dense, e_send);
   ConnCounters* cr = conn_at(a, dense, e_recv);
@@ -299,6 +336,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   const int64_t step_bytes = g.step_bytes;
   const T* in = reinterpret_cast<const T*>(a.send[rank]);
   T* out = reinterpret_cast<T*>(a.recv[rank]);
+  const bool direct = a.direct != 0;
+  T* next_out = reinterpret_cast<T*>(a.recv[next_rank_of(a, dense, ring_idx)]);
   SliceCursor c;
   cursor_begin(g, dense, ring_idx, c);
 
@@ -317,7 +356,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
           if (sp.poll(a, info | (2u << 24) | i, rstep + sps)) { sh_abort = 1; break; }
         }
       }
-      if (!sh_abort && row_sends(c.prim)) {
+      if (!sh_abort && row_sends(c.prim) && !direct_send_row(direct, c.prim)) {  // direct sends fill no slot
         Spin sp;
         // Until the receiver's first release in this call, its head may still
         // hold the previous call's final step (< base_send): all slots free.
@@ -347,6 +386,10 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       const int prim = c.prim;
       const bool has_in = prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend;
       const bool has_rcv = row_recvs(prim);
+      // direct mode: a forwarded final is staged from this rank's own output,
+      // the last row moves nothing
+      const bool rcv_own_out = direct_recv_row(direct, prim);
+      const bool rcv_bytes = has_rcv && !(rcv_own_out && prim == kRecv);
       const int rcv_eb = recv_is_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       if (has_rcv) fence_proxy_async_global();  // the tail acquired above, before bulk reads of the FIFO
@@ -361,12 +404,14 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         const int ne = (int)imin(kTileElems, c.nelem - e0);
         const int covered = ne / P * P;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
-        const uint32_t b_rcv = has_rcv ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
+        const uint32_t b_rcv = rcv_bytes ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
         char* s_in = smem + (int64_t)st * SB;
         char* s_rcv = s_in + kTileElems * (int)sizeof(T);
         mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
         if (b_in) tma_load_1d(s_in, in + c.offset + e0, b_in, &bar_full[st], pol);
-        if (b_rcv) tma_load_1d(s_rcv, rslot + e0 * rcv_eb, b_rcv, &bar_full[st], pol);
+        if (b_rcv)
+          tma_load_1d(s_rcv, rcv_own_out ? reinterpret_cast<const char*>(out + c.offset + e0) : rslot + e0 * rcv_eb,
+                      b_rcv, &bar_full[st], pol);
         gt++;
       }
       if (has_rcv) rstep += sps;
@@ -435,7 +480,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         const int ne = (int)imin(kTileElems, c.nelem - e0);
         const char* s_in = smem + (int64_t)st * SB;
         const char* s_rcv = s_in + kTileElems * (int)sizeof(T);
-        tile_compute_any<T>(c.prim, s_in, s_rcv, in + c.offset, out + c.offset, rslot, sslot, e0, ne, ne / P * P,
+        tile_compute_any<T>(direct, c.prim, s_in, s_rcv, in + c.offset, out + c.offset, next_out + c.offset, rslot,
+                            sslot, e0, ne, ne / P * P,
                             ct, kComputeThreads, out_pol);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);

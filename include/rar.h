@@ -136,6 +136,36 @@ RAR_API rar_status rar_allreduce(const void* const* sendbufs, void* const* recvb
                          uint64_t channelMask, rar_proto proto, size_t buffSize, int chunkSteps,
                          void* workspace, size_t workspaceBytes, void* stream);
 
+/* Flags of rar_allreduce_ex. */
+#define RAR_FLAG_DIRECT 1u /* Simple: all-gather hops write the next rank's output directly */
+
+/*
+ * rar_allreduce with one ring order per channel and with options.
+ *
+ * ring_orders: host array of nrings x nranks user ranks; nrings is 1 (every
+ *   channel uses the same ring, as in rar_allreduce) or popcount(channelMask)
+ *   (dense channel n uses ring n, as NCCL gives each channel its own ring
+ *   permutation: [C12] "GRAPH 重建：N=4", "为什么 channels 会重复"). Each ring
+ *   must be a permutation of 0..nranks-1, else RAR_ERR_RING; another nrings
+ *   is RAR_ERR_ARG. Ring orders may change from call to call on one workspace.
+ * flags: 0 or RAR_FLAG_DIRECT (Simple only, else RAR_ERR_ARG). With
+ *   RAR_FLAG_DIRECT the all-gather hops use direct writes ([C23] "发布顺序与
+ *   Fence": direct read/write skip FIFO slots, barriers and progress stay): a
+ *   rank that sends a final value stores it straight into the next rank's
+ *   receive buffer and publishes its tail; the receiver waits for the tail and
+ *   forwards from its own receive buffer. No FIFO slot is used for those hops,
+ *   so the sender takes no credit for them. The result is identical to the
+ *   FIFO path. In place stays allowed (a rank's input chunk is always read
+ *   before any peer's direct write to it, since each chunk's partial sum passes
+ *   through every rank first).
+ * Every other argument, and every error, as for rar_allreduce.
+ */
+RAR_API rar_status rar_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                                    size_t count, rar_dtype dtype, rar_redop op,
+                                    const int* ring_orders, int nrings, uint64_t channelMask,
+                                    rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags,
+                                    void* workspace, size_t workspaceBytes, void* stream);
+
 /*
  * One-shot AllReduce (sum) over nranks virtual ranks ([OS89], the single
  * kernel form; [NOTES] "5 Symmetric Memory": a rank reads its peers' buffers

@@ -128,3 +128,26 @@ def test_library_geometry_matches_oracle(lib, seed):
     for ch in range(got["nchannels"]):
         loops = oracle.channel_loops(_oracle_proto(proto), int(dtype), n, mask, count, ch, bs, cs)
         assert got["loops"][ch] == len(loops)
+
+
+def call_ex(n=4, rings=None, nrings=None, mask=0b11, proto=B.Proto.SIMPLE, flags=0, count=1024, ws=FAKE, wsb=1 << 30):
+    rings = [list(range(n))] if rings is None else rings
+    flat = [v for r in rings for v in r]
+    nrings = len(rings) if nrings is None else nrings
+    L = B.load_library()
+    sp = (ctypes.c_void_p * n)(*[FAKE + (i << 28) for i in range(n)])
+    rp = (ctypes.c_void_p * n)(*[FAKE + (1 << 35) + (i << 28) for i in range(n)])
+    rg = (ctypes.c_int * len(flat))(*flat)
+    return L.rar_allreduce_ex(sp, rp, n, count, 0, 0, rg, nrings, mask, int(proto), 65536, 4, flags, ws, wsb, None)
+
+
+def test_allreduce_ex_argument_errors(lib):
+    S = B.Status
+    assert call_ex(count=0) == S.OK
+    assert call_ex(rings=[[0, 1, 2, 3], [0, 2, 1, 3]], count=0) == S.OK  # one ring per channel
+    assert call_ex(rings=[[0, 1, 2, 3]] * 3) == S.ERR_ARG  # 3 rings for 2 channels
+    assert call_ex(rings=[[0, 1, 2, 3], [0, 1, 1, 3]]) == S.ERR_RING
+    assert call_ex(flags=1, proto=B.Proto.LL) == S.ERR_ARG  # direct is Simple only
+    assert call_ex(flags=1, count=0) == S.OK
+    assert call_ex(flags=2) == S.ERR_ARG
+    assert call_ex(wsb=16) == S.ERR_WORKSPACE
