@@ -64,19 +64,21 @@ def wire_factor(proto):
     return {"Simple": 1.0, "LL128": 16.0 / 15.0, "LL": 2.0}[proto]
 
 
-def algorithmic_bytes(case):
+def algorithmic_bytes(case, direct=False):
     """Ideal bytes of one call: every rank reads its input and writes its output
     once (N * 2S), plus each FIFO byte written once and read once, 2(N-1)/N * S
     per rank on the wire (LL doubles it, LL128 adds 1/15). bf16 partial sums
-    cross the reduce-scatter half as binary32."""
+    cross the reduce-scatter half as binary32. Direct all-gather: only the
+    reduce-scatter half uses the FIFO; each rank reads back the (N-2) chunks it
+    forwards from its own output."""
     n = case.nranks
     s = case.count * (4 if case.dtype == "f32" else 2)
     w = wire_factor(case.proto)
-    if case.dtype == "f32":
-        fifo = n * 2 * (2 * (n - 1) / n * s * w)
-    else:
-        fifo = n * 2 * ((n - 1) / n * 2 * s * w + (n - 1) / n * s * w)
-    return n * 2 * s + fifo
+    rs = (n - 1) / n * s * (2 if case.dtype == "bf16" else 1) * w
+    ag = (n - 1) / n * s * w
+    if direct:
+        return n * 2 * s + n * 2 * rs + n * (n - 2) / n * s
+    return n * 2 * s + n * 2 * (rs + ag)
 
 
 def measured_peak():
@@ -153,7 +155,7 @@ def device_inputs(case, torch):
     return x
 
 
-def time_ring(case, torch, B, steps, warmup):
+def time_ring(case, torch, B, steps, warmup, direct=False):
     """Device time per call (CUDA events on the launching stream)."""
     x = device_inputs(case, torch)
     y = torch.empty_like(x)
@@ -161,13 +163,17 @@ def time_ring(case, torch, B, steps, warmup):
     recv = [y[r] for r in range(case.nranks)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
     stream = torch.cuda.current_stream()
+    def call():
+        B.allreduce_ex(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps,
+                       direct=direct)
+
     for _ in range(warmup):
-        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+        call()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for a, b in ev:
         a.record(stream)
-        B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size, case.chunk_steps)
+        call()
         b.record(stream)
     torch.cuda.synchronize()
     st = B.get_status(ws)
@@ -184,13 +190,15 @@ def sweep(torch, B, steps, warmup, peak):
     cases = gen.large_cases()
     cases.append(gen.RingCase("n8_ll_ch12_64MiB", 8, cases[0].ring, 0xFFF, gen.LL, 64 * gen.MIB // 4,
                               gen.F32, "normal", 3, 0, 4))
-    for c in cases:
-        ms = time_ring(c, torch, B, steps, warmup)
+    runs = [(c, False) for c in cases] + [(c, True) for c in cases if c.proto == gen.SIMPLE]
+    for c, direct in runs:
+        ms = time_ring(c, torch, B, steps, warmup, direct)
         t = statistics.median(ms) / 1e3
-        out[c.name] = {"busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
-                       "us": round(t * 1e6, 1),
-                       "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3),
-                       "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
+        out[c.name + ("_direct_allgather" if direct else "")] = {
+            "busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
+            "us": round(t * 1e6, 1),
+            "roofline_frac": round(algorithmic_bytes(c, direct) / t / 1e9 / peak, 3),
+            "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
     # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel. Device
     # latency from a CUDA graph of back-to-back calls (no host enqueue time),
     # and the stream-launch latency as seen between two events.
