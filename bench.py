@@ -496,6 +496,39 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_oneshot_only(args):
+    """Time only the one-shot AllReduce: N=8 bf16 ranks, 7168 x T elements each
+    (T = --oneshot-tokens), CUDA events around each call, one JSON line."""
+    import torch
+    from collective_communication_gb300 import binding as B
+    from collective_communication_gb300 import inputs as gen
+    B.load_library()
+    peak, _ = measured_peak()
+    case = gen.OneShotCase(f"oneshot_bf16_n8_7168x{args.oneshot_tokens}", 8, 7168 * args.oneshot_tokens)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(case.seed)
+    x = torch.randn((8, case.count), generator=g, device="cuda").to(torch.bfloat16)
+    y = torch.empty_like(x)
+    send = [x[r] for r in range(8)]
+    recv = [y[r] for r in range(8)]
+    for _ in range(args.warmup):
+        B.oneshot(send, recv)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(s)
+        B.oneshot(send, recv)
+        b.record(s)
+    torch.cuda.synchronize()
+    t = statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
+    unique = 2 * 8 * case.count * 2
+    print(json.dumps({"metric": "one-shot AllReduce time", "value": round(t * 1e6, 2), "unit": "us",
+                      "higher_is_better": False, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
+                      "config": {"workload": case.name},
+                      "unique_bytes_frac": round(unique / t / 1e9 / peak, 3)}))
+
+
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is one step-by-step
     simulation of the whole headline call, single-threaded."""
@@ -548,11 +581,14 @@ def main():
     ap.add_argument("--mib", type=int, help="MiB per rank")
     ap.add_argument("--nranks", type=int)
     ap.add_argument("--channels", type=int)
+    ap.add_argument("--oneshot-tokens", type=int, help="time only the one-shot AllReduce of 7168 x T bf16")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.oneshot_tokens:
+        run_oneshot_only(args)
     else:
         run_gpu(args)
 

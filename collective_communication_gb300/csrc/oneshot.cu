@@ -21,7 +21,7 @@
 namespace rar {
 
 constexpr int kOneShotThreads = 256;
-constexpr int kOneShotUnroll = 2;
+constexpr int kOneShotUnroll = 1;  // low register count: more resident warps per SM
 
 template <typename T>
 struct OsPack;
