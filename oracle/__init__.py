@@ -1,6 +1,7 @@
-"""CPU oracle for the ring AllReduce over N virtual ranks (and the one-shot
-variant): a plain, slow, step-by-step C implementation plus the closed form of
-its result.
+"""CPU oracle for the ring AllReduce over N virtual ranks, its two halves
+(ReduceScatter, AllGather) as collectives of their own, and the one-shot
+variant: a plain, slow, step-by-step C implementation plus the closed form of
+each result.
 
 TEST INFRASTRUCTURE. Only tests/, the smoke check in __graft_entry__ and the
 CPU-baseline leg of bench.py may import this package. The product (the CUDA
@@ -25,14 +26,17 @@ F32, BF16 = 0, 1
 LL, LL128, SIMPLE = 0, 1, 2
 PROTO_NAMES = {LL: "LL", LL128: "LL128", SIMPLE: "Simple"}
 OK, EARG, ERING, EDEADLOCK, ECHECK, ENOMEM = range(6)
-SEND, RECV_REDUCE_SEND, RECV_REDUCE_COPY_SEND, RECV_COPY_SEND, RECV = range(5)
+SEND, RECV_REDUCE_SEND, RECV_REDUCE_COPY_SEND, RECV_COPY_SEND, RECV, RECV_REDUCE_COPY, COPY_SEND = range(7)
 PRIM_NAMES = {
     SEND: "send",
     RECV_REDUCE_SEND: "recvReduceSend",
     RECV_REDUCE_COPY_SEND: "directRecvReduceCopySend",
     RECV_COPY_SEND: "directRecvCopySend",
     RECV: "directRecv",
+    RECV_REDUCE_COPY: "recvReduceCopy",
+    COPY_SEND: "copySend",
 }
+ALLREDUCE, REDUCE_SCATTER, ALL_GATHER = 0, 1, 2
 M_COMPLETE, M_STALL, M_CORRUPT = 0, 1, 2
 
 _lib = None
@@ -52,6 +56,7 @@ def lib():
         P, I, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_size_t
         L.orc_ring_setup.argtypes = [I, P, P, P, P, P]
         L.orc_schedule.argtypes = [I, I, P, P]
+        L.orc_schedule_kind.argtypes = [I, I, I, P, P]
         L.orc_mask_channels.argtypes = [U64, P]
         L.orc_default_buffsize.argtypes = [I]
         L.orc_default_buffsize.restype = SZ
@@ -66,6 +71,8 @@ def lib():
         L.orc_ll128_decode.restype = SZ
         L.orc_ring_allreduce_sim.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I, I, P, P, P]
         L.orc_ring_allreduce_closed.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I]
+        L.orc_ring_collective_sim.argtypes = [I, P, P, I, SZ, I, P, I, U64, I, SZ, I, I, P, P, P]
+        L.orc_ring_halves_closed.argtypes = [I, P, P, I, SZ, I, P, I, U64, I, SZ, I]
         L.orc_ring_closed_at.argtypes = [P, I, SZ, I, P, I, U64, I, SZ, I, P, SZ, P, P]
         L.orc_oneshot.argtypes = [P, P, I, SZ, I]
         L.orc_state_model.argtypes = [I, I, I, I, P]
@@ -261,6 +268,58 @@ def ring_closed_at(sampled, ring_order, mask, proto, idx, count, buff_size=0, ch
                                   _ptr(chunks))
     _check(st, "ring_closed_at")
     return out, chunks
+
+
+def schedule_kind(kind, n, ring_index):
+    """Rows (primitive, chunk) of one collective kind for the rank at ring_index."""
+    prim = np.zeros(2 * n, np.int32)
+    chunk = np.zeros(2 * n, np.int32)
+    rows = lib().orc_schedule_kind(kind, n, ring_index, _ptr(prim), _ptr(chunk))
+    if rows < 0:
+        raise OracleError(rows, "schedule_kind")
+    return [(int(p), int(c)) for p, c in zip(prim[:rows], chunk[:rows])]
+
+
+def _half_buffers(kind, inputs):
+    ins, dt = _prep(inputs)
+    n = len(ins)
+    if kind == REDUCE_SCATTER:
+        if ins[0].size % n:
+            raise ValueError("a ReduceScatter input holds nranks blocks")
+        count = ins[0].size // n
+        outs = [np.zeros(count, ins[0].dtype) for _ in ins]
+    elif kind == ALL_GATHER:
+        count = ins[0].size
+        outs = [np.zeros(n * count, ins[0].dtype) for _ in ins]
+    else:
+        raise ValueError("kind must be REDUCE_SCATTER or ALL_GATHER")
+    return ins, dt, n, count, outs
+
+
+def ring_halves_sim(kind, inputs, ring_order, mask, proto, buff_size=0, chunk_steps=4, direct=False):
+    """Step-by-step simulation of a ReduceScatter (inputs of nranks*count
+    elements, outputs of count) or an AllGather (inputs of count, outputs of
+    nranks*count). Returns (outputs, sends, recvs, loops per channel)."""
+    ins, dt, n, count, outs = _half_buffers(kind, inputs)
+    sends = np.zeros(n, np.int64)
+    recvs = np.zeros(n, np.int64)
+    loops = np.zeros(64, np.int64)
+    rings, nrings = _rings(ring_order)
+    st = lib().orc_ring_collective_sim(kind, _ptr_array(ins), _ptr_array(outs), n, count, dt, _ptr(rings),
+                                       nrings, mask, proto, buff_size, chunk_steps, int(direct),
+                                       _ptr(sends), _ptr(recvs), _ptr(loops))
+    _check(st, "ring_halves_sim")
+    return outs, sends, recvs, loops[:len(mask_channels(mask))]
+
+
+def ring_halves_closed(kind, inputs, ring_order, mask, proto, buff_size=0, chunk_steps=4):
+    """Closed form of a ReduceScatter or an AllGather (shapes as in ring_halves_sim)."""
+    ins, dt, n, count, outs = _half_buffers(kind, inputs)
+    rings, nrings = _rings(ring_order)
+    st = lib().orc_ring_halves_closed(kind, _ptr_array(ins), _ptr_array(outs), n, count, dt, _ptr(rings),
+                                      nrings, mask, proto, buff_size, chunk_steps)
+    _check(st, "ring_halves_closed")
+    return outs
 
 
 def oneshot(inputs):

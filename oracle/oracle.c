@@ -51,8 +51,14 @@ enum {
   ORC_RECV_REDUCE_SEND = 1,
   ORC_RECV_REDUCE_COPY_SEND = 2,
   ORC_RECV_COPY_SEND = 3,
-  ORC_RECV = 4
+  ORC_RECV = 4,
+  /* the halves as collectives of their own ([C12] "源码步骤三": the owner row is
+   * the last recv+reduce of ReduceScatter fused with the first send of AllGather) */
+  ORC_RECV_REDUCE_COPY = 5, /* ReduceScatter's last row: recv + reduce, write the output */
+  ORC_COPY_SEND = 6         /* AllGather's first row: copy the input to the output and send it */
 };
+/* Collective run on the ring ([C12] "Ring AllReduce 不只是“绕一圈”"). */
+enum { ORC_ALLREDUCE = 0, ORC_REDUCE_SCATTER = 1, ORC_ALL_GATHER = 2 };
 
 static size_t div_up(size_t a, size_t b) { return (a + b - 1) / b; }
 static size_t align_up(size_t a, size_t b) { return div_up(a, b) * b; }
@@ -186,6 +192,29 @@ static int prim_of_row(int n, int s) {
 
 static int chunk_of_row(int n, int i, int s) { return ((i - s - 1) % n + 2 * n) % n; }
 
+/*
+ * The halves on their own, n rows each (reading: the AllReduce rows split at
+ * the owner row, whose recv+reduce ends ReduceScatter and whose send starts
+ * AllGather, [C12] "源码步骤三"):
+ *   ReduceScatter  s = 0 send, s = 1..n-2 recvReduceSend, s = n-1 recvReduceCopy;
+ *                  chunk (i-s-1) mod n, as in the AllReduce rows 0..n-1.
+ *   AllGather      s = 0 copySend, s = 1..n-2 recvCopySend, s = n-1 recv;
+ *                  chunk (i-s) mod n, as in the AllReduce rows n-1..2n-2.
+ */
+static int rows_of_kind(int kind, int n) { return kind == ORC_ALLREDUCE ? 2 * n - 1 : n; }
+
+static int prim_of_kind_row(int kind, int n, int s) {
+  if (kind == ORC_REDUCE_SCATTER)
+    return s == 0 ? ORC_SEND : s < n - 1 ? ORC_RECV_REDUCE_SEND : ORC_RECV_REDUCE_COPY;
+  if (kind == ORC_ALL_GATHER) return s == 0 ? ORC_COPY_SEND : s < n - 1 ? ORC_RECV_COPY_SEND : ORC_RECV;
+  return prim_of_row(n, s);
+}
+
+static int chunk_of_kind_row(int kind, int n, int i, int s) {
+  if (kind == ORC_ALL_GATHER) return ((i - s) % n + 2 * n) % n;
+  return chunk_of_row(n, i, s);
+}
+
 int orc_schedule(int n, int ring_index, int* prim, int* chunk) {
   if (n < 1 || ring_index < 0 || ring_index >= n) return ORC_EARG;
   if (n == 1) return ORC_EARG;
@@ -196,6 +225,18 @@ int orc_schedule(int n, int ring_index, int* prim, int* chunk) {
   return ORC_OK;
 }
 
+/* Rows of one collective kind; returns the row count, or -1. */
+int orc_schedule_kind(int kind, int n, int ring_index, int* prim, int* chunk) {
+  if (kind < ORC_ALLREDUCE || kind > ORC_ALL_GATHER) return -1;
+  if (n < 2 || ring_index < 0 || ring_index >= n) return -1;
+  int rows = rows_of_kind(kind, n);
+  for (int s = 0; s < rows; s++) {
+    prim[s] = prim_of_kind_row(kind, n, s);
+    chunk[s] = chunk_of_kind_row(kind, n, ring_index, s);
+  }
+  return rows;
+}
+
 /* ------------------------------------------------------------------ */
 /* Geometry ([C23] "Kernel 如何把 Block 映射到 Channel",                */
 /*           "Buffer 到 Chunk 的实测公式", "Slice Size", "LL", "LL128"; */
@@ -203,9 +244,10 @@ int orc_schedule(int n, int ring_index, int* prim, int* chunk) {
 /* ------------------------------------------------------------------ */
 
 typedef struct {
+  int kind;             /* ORC_ALLREDUCE, ORC_REDUCE_SCATTER or ORC_ALL_GATHER */
   int proto, dtype, nranks, nchan;
   int chan_id[MAXCH];   /* dense channel n -> channel id */
-  size_t count;         /* elements per rank */
+  size_t count;         /* elements per rank (AllReduce) or per rank block (the halves) */
   size_t elem_bytes;    /* sizeof(T) */
   size_t align_elems;   /* 16 / sizeof(T) */
   size_t step_bytes;    /* FIFO bytes per step (line bytes for LL and LL128) */
@@ -303,11 +345,19 @@ static void channel_range(const geom_t* g, int n, size_t* gridOffset, size_t* ch
   *channelCount = off >= g->count ? 0 : min_sz(g->per_channel, g->count - off);
 }
 
+/* Elements of a channel's range one loop covers. AllReduce: n chunks of the
+ * rank's buffer. Reading (the halves): the channel range is a range of every
+ * rank block, and one loop moves one chunk of it from every block. */
+static size_t loop_count_of(const geom_t* g) {
+  return g->kind == ORC_ALLREDUCE ? (size_t)g->nranks * g->chunk_elems : g->chunk_elems;
+}
+
 /* Per-loop chunk size: full chunks, except in the last, short loop where the
  * remainder is split over the n ranks and aligned up to 16/sizeof(T)
- * ([C12] "runRing 的数据切分"). */
+ * ([C12] "runRing 的数据切分"). The halves: the remainder, at most a chunk. */
 static size_t loop_chunk_count(const geom_t* g, size_t remCount) {
-  size_t loopCount = (size_t)g->nranks * g->chunk_elems;
+  if (g->kind != ORC_ALLREDUCE) return min_sz(remCount, g->chunk_elems);
+  size_t loopCount = loop_count_of(g);
   if (remCount < loopCount) return align_up(div_up(remCount, (size_t)g->nranks), g->align_elems);
   return g->chunk_elems;
 }
@@ -478,7 +528,8 @@ typedef struct {
 /* One slice of one rank's program. */
 typedef struct {
   int prim;
-  size_t offset; /* user element offset of the slice */
+  size_t in_el;  /* element of the rank's input where the slice starts */
+  size_t out_el; /* element of the rank's output where the slice starts */
   size_t nelem;
 } slice_t;
 
@@ -489,10 +540,10 @@ typedef struct {
  */
 static int sends_partial(int prim) { return prim == ORC_SEND || prim == ORC_RECV_REDUCE_SEND; }
 static int recvs_partial(int prim) {
-  return prim == ORC_RECV_REDUCE_SEND || prim == ORC_RECV_REDUCE_COPY_SEND;
+  return prim == ORC_RECV_REDUCE_SEND || prim == ORC_RECV_REDUCE_COPY_SEND || prim == ORC_RECV_REDUCE_COPY;
 }
-static int has_recv(int prim) { return prim != ORC_SEND; }
-static int has_send(int prim) { return prim != ORC_RECV; }
+static int has_recv(int prim) { return prim != ORC_SEND && prim != ORC_COPY_SEND; }
+static int has_send(int prim) { return prim != ORC_RECV && prim != ORC_RECV_REDUCE_COPY; }
 
 static size_t payload_bytes(const geom_t* g, int partial, size_t nelem) {
   return nelem * (partial ? 4 : g->elem_bytes);
@@ -579,44 +630,51 @@ static int sim_try_slice(sim_t* S, int i, const slice_t* sl) {
    * slot, then publishes the tail as usual; its receiver waits for the tail and
    * finds the value already in its own output. No slot is filled, so the
    * sender skips the credit wait; the step counters advance as before. */
-  int direct_send = S->direct && (prim == ORC_RECV_REDUCE_COPY_SEND || prim == ORC_RECV_COPY_SEND);
+  /* AllGather's first row sends a final value too, so it writes directly as well. */
+  int direct_send = S->direct && (prim == ORC_RECV_REDUCE_COPY_SEND || prim == ORC_RECV_COPY_SEND ||
+                                  prim == ORC_COPY_SEND);
   int direct_recv = S->direct && (prim == ORC_RECV_COPY_SEND || prim == ORC_RECV);
   int r_next = S->rank_at[(i + 1) % n];
   if (has_send(prim) && !direct_send && !fifo_can_send(S, e_send, S->sstep[i])) return 0;
   if (direct_recv) {
     if (S->conn[e_recv].tail < S->rstep[i] + (uint64_t)g->sps) return 0;
-    for (size_t j = 0; j < nelem; j++) S->vals[j] = load_as_f32(S->recv[r], g->dtype, sl->offset + j);
+    for (size_t j = 0; j < nelem; j++) S->vals[j] = load_as_f32(S->recv[r], g->dtype, sl->out_el + j);
   } else if (has_recv(prim)) {
     size_t nb = payload_bytes(g, recvs_partial(prim), nelem);
     if (!fifo_try_recv(S, e_recv, S->rstep[i], nb)) return 0;
     unpack_values(g, recvs_partial(prim), S->pay_in, nelem, S->vals);
   }
-  /* The arithmetic of the five primitives ([C12] "源码步骤一..五"). */
+  /* The arithmetic of the primitives ([C12] "源码步骤一..五"). */
   for (size_t j = 0; j < nelem; j++) {
-    size_t el = sl->offset + j;
-    float x = load_as_f32(S->send[r], g->dtype, el);
+    size_t ie = sl->in_el + j, oe = sl->out_el + j;
     switch (prim) {
       case ORC_SEND:
-        S->vals[j] = x; /* the raw local input, no reduction */
+        S->vals[j] = load_as_f32(S->send[r], g->dtype, ie); /* the raw local input, no reduction */
         break;
       case ORC_RECV_REDUCE_SEND:
-        S->vals[j] = S->vals[j] + x;
+        S->vals[j] = S->vals[j] + load_as_f32(S->send[r], g->dtype, ie);
         break;
-      case ORC_RECV_REDUCE_COPY_SEND: {
-        float v = S->vals[j] + x; /* the last reduction of this chunk */
-        store_from_f32(S->recv[r], g->dtype, el, v); /* rounded once for bf16 */
-        S->vals[j] = load_as_f32(S->recv[r], g->dtype, el); /* forward the stored value */
+      case ORC_RECV_REDUCE_COPY_SEND:
+      case ORC_RECV_REDUCE_COPY: {
+        float v = S->vals[j] + load_as_f32(S->send[r], g->dtype, ie); /* the last reduction */
+        store_from_f32(S->recv[r], g->dtype, oe, v); /* rounded once for bf16 */
+        S->vals[j] = load_as_f32(S->recv[r], g->dtype, oe); /* forward the stored value */
         break;
       }
+      case ORC_COPY_SEND:
+        S->vals[j] = load_as_f32(S->send[r], g->dtype, ie);
+        store_from_f32(S->recv[r], g->dtype, oe, S->vals[j]); /* exact: the value is already T */
+        break;
       case ORC_RECV_COPY_SEND:
       case ORC_RECV:
-        if (!direct_recv) store_from_f32(S->recv[r], g->dtype, el, S->vals[j]);
+        if (!direct_recv) store_from_f32(S->recv[r], g->dtype, oe, S->vals[j]);
         break;
     }
   }
   if (has_send(prim)) {
     if (direct_send) {
-      for (size_t j = 0; j < nelem; j++) store_from_f32(S->recv[r_next], g->dtype, sl->offset + j, S->vals[j]);
+      /* the same block offset in the next rank's output */
+      for (size_t j = 0; j < nelem; j++) store_from_f32(S->recv[r_next], g->dtype, sl->out_el + j, S->vals[j]);
       S->conn[e_send].tail = S->sstep[i] + (uint64_t)g->sps; /* data first, then the tail */
     } else {
       size_t nb = payload_bytes(g, sends_partial(prim), nelem);
@@ -640,24 +698,41 @@ static int sim_try_slice(sim_t* S, int i, const slice_t* sl) {
   return 1;
 }
 
-/* The program of the rank at ring index i on one channel: loops x rows x slices. */
-static size_t build_program(const geom_t* g, int i, size_t gridOffset, size_t channelCount,
-                            slice_t* prog) {
+/*
+ * The program of the rank at ring index i on one channel: loops x rows x
+ * slices. AllReduce: chunk c of a loop is a piece of every rank's buffer, at
+ * the same offset in input and output. The halves (reading, the collectives'
+ * usual shapes): a ReduceScatter input and an AllGather output hold n blocks
+ * of `count` elements, block b belonging to user rank b; a chunk with ring
+ * index c is the loop's range of the block of user rank rank_at[c], and the
+ * other side (ReduceScatter output, AllGather input) holds one block.
+ */
+static size_t build_program(const geom_t* g, const int* rank_at, int i, size_t gridOffset,
+                            size_t channelCount, slice_t* prog) {
   int n = g->nranks;
-  size_t loopCount = (size_t)n * g->chunk_elems;
+  size_t loopCount = loop_count_of(g);
   size_t k = 0;
   for (size_t elemOffset = 0; elemOffset < channelCount; elemOffset += loopCount) {
     size_t rem = channelCount - elemOffset;
     size_t chunkCount = loop_chunk_count(g, rem);
-    for (int s = 0; s < 2 * n - 1; s++) {
-      int c = chunk_of_row(n, i, s);
-      size_t nelem = chunk_nelem(chunkCount, rem, c);
+    for (int s = 0; s < rows_of_kind(g->kind, n); s++) {
+      int c = chunk_of_kind_row(g->kind, n, i, s);
+      size_t nelem, base;
+      if (g->kind == ORC_ALLREDUCE) {
+        nelem = chunk_nelem(chunkCount, rem, c);
+        base = gridOffset + elemOffset + chunkCount * (size_t)c;
+      } else {
+        nelem = chunkCount;
+        base = gridOffset + elemOffset;
+      }
+      size_t blk = (size_t)rank_at[c] * g->count;
       size_t ss = slice_size(g, nelem);
       for (int q = 0; q < g->spc; q++) {
         size_t so = ss * (size_t)q;
         slice_t sl;
-        sl.prim = prim_of_row(n, s);
-        sl.offset = gridOffset + elemOffset + chunkCount * (size_t)c + so;
+        sl.prim = prim_of_kind_row(g->kind, n, s);
+        sl.in_el = base + so + (g->kind == ORC_REDUCE_SCATTER ? blk : 0);
+        sl.out_el = base + so + (g->kind == ORC_ALL_GATHER ? blk : 0);
         sl.nelem = nelem > so ? min_sz(ss, nelem - so) : 0; /* empty slices still run */
         if (prog) prog[k] = sl;
         k++;
@@ -668,24 +743,30 @@ static size_t build_program(const geom_t* g, int i, size_t gridOffset, size_t ch
 }
 
 /*
- * Step-by-step simulation of one ring AllReduce call over all channels.
- * send[r], recv[r]: per user rank buffers of `count` elements (binary32, or
- * bf16 bit patterns). sends/recvs (optional, per user rank) count the slices
- * each rank sent and received; loops_out (optional, per dense channel) the
- * chunk loops of each channel.
+ * Step-by-step simulation of one ring collective call over all channels.
+ * kind: ORC_ALLREDUCE (send[r], recv[r]: `count` elements), ORC_REDUCE_SCATTER
+ * (send[r]: nranks*count, recv[r]: count) or ORC_ALL_GATHER (send[r]: count,
+ * recv[r]: nranks*count); elements are binary32 or bf16 bit patterns.
+ * sends/recvs (optional, per user rank) count the slices each rank sent and
+ * received; loops_out (optional, per dense channel) the chunk loops of each
+ * channel.
  * Ranks are run round-robin; each runs its next slices until a wait is not
  * met. When a full round makes no progress while work remains, the result is
  * ORC_EDEADLOCK.
  */
-int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nranks, size_t count,
-                           int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
-                           size_t buffSize, int chunkSteps, int direct, int64_t* sends, int64_t* recvs,
-                           int64_t* loops_out) {
+int orc_ring_collective_sim(int kind, const void* const* send, void* const* recv, int nranks, size_t count,
+                            int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
+                            size_t buffSize, int chunkSteps, int direct, int64_t* sends, int64_t* recvs,
+                            int64_t* loops_out) {
   geom_t g;
+  if (kind < ORC_ALLREDUCE || kind > ORC_ALL_GATHER) return ORC_EARG;
   int st = geom_init(&g, proto, dtype, nranks, mask, count, buffSize, chunkSteps);
   if (st != ORC_OK) return st;
+  g.kind = kind;
   if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
   if (direct && proto != ORC_SIMPLE) return ORC_EARG;
+  /* ReduceScatter has no hop that carries a final value: nothing to write directly */
+  if (direct && kind == ORC_REDUCE_SCATTER) return ORC_EARG;
   int rank_at[MAXR];
   for (int ch = 0; ch < nrings; ch++) {
     st = rank_at_index(nranks, ring_order + (size_t)ch * nranks, rank_at);
@@ -735,17 +816,14 @@ int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nrank
     size_t nslices = 0;
     for (int i = 0; i < nranks; i++) {
       S.sstep[i] = S.rstep[i] = 0;
-      nslices = build_program(&g, i, gridOffset, channelCount, NULL);
+      nslices = build_program(&g, rank_at, i, gridOffset, channelCount, NULL);
       free(prog[i]);
       prog[i] = malloc(sizeof(slice_t) * (nslices ? nslices : 1));
       if (!prog[i]) { rc = ORC_ENOMEM; goto done; }
-      build_program(&g, i, gridOffset, channelCount, prog[i]);
+      build_program(&g, rank_at, i, gridOffset, channelCount, prog[i]);
       cursor[i] = 0;
     }
-    if (loops_out) {
-      size_t loopCount = (size_t)nranks * g.chunk_elems;
-      loops_out[ch] = (int64_t)div_up(channelCount, loopCount);
-    }
+    if (loops_out) loops_out[ch] = (int64_t)div_up(channelCount, loop_count_of(&g));
     int finished = 0;
     while (finished < nranks) {
       int progressed = 0;
@@ -774,6 +852,14 @@ done:
   free(pout);
   free(vals);
   return rc;
+}
+
+int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nranks, size_t count,
+                           int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
+                           size_t buffSize, int chunkSteps, int direct, int64_t* sends, int64_t* recvs,
+                           int64_t* loops_out) {
+  return orc_ring_collective_sim(ORC_ALLREDUCE, send, recv, nranks, count, dtype, ring_order, nrings, mask,
+                                 proto, buffSize, chunkSteps, direct, sends, recvs, loops_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -822,6 +908,48 @@ int orc_ring_allreduce_closed(const void* const* send, void* const* recv, int nr
         for (size_t j = 0; j < nelem; j++) {
           float v = ring_fold(&g, send, rank_at, c, base + j);
           for (int r = 0; r < nranks; r++) store_from_f32(recv[r], dtype, base + j, v);
+        }
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/*
+ * Closed form of the halves ([C12] "Ring AllReduce 不只是“绕一圈”": AllReduce is
+ * ReduceScatter followed by AllGather).
+ * ReduceScatter: element j of rank r's output is block r, element j, folded
+ *   along the ring of j's channel exactly as an AllReduce chunk whose owner is
+ *   r: it starts at the rank after r on the ring and ends with r's own input,
+ *     out_r[j] = T(x[c+1][r*count+j] + x[c+2][r*count+j] + ... + x[c][r*count+j])
+ *   with c the ring index of r and x[i] the input of the rank at ring index i.
+ * AllGather: out_r[q*count + j] = in_q[j] for every pair of ranks (a copy).
+ * The channel of element j is the one whose range of the block holds j.
+ */
+int orc_ring_halves_closed(int kind, const void* const* send, void* const* recv, int nranks, size_t count,
+                           int dtype, const int* ring_order, int nrings, uint64_t mask, int proto,
+                           size_t buffSize, int chunkSteps) {
+  geom_t g;
+  if (kind != ORC_REDUCE_SCATTER && kind != ORC_ALL_GATHER) return ORC_EARG;
+  int st = geom_init(&g, proto, dtype, nranks, mask, count, buffSize, chunkSteps);
+  if (st != ORC_OK) return st;
+  g.kind = kind;
+  if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
+  int rank_at[MAXR], index[MAXR];
+  for (int ch = 0; ch < g.nchan; ch++) {
+    st = rank_at_index(nranks, ring_order + (nrings == 1 ? 0 : (size_t)ch * nranks), rank_at);
+    if (st != ORC_OK) return st;
+    for (int c = 0; c < nranks; c++) index[rank_at[c]] = c;
+    size_t gridOffset, channelCount;
+    channel_range(&g, ch, &gridOffset, &channelCount);
+    for (size_t j = gridOffset; j < gridOffset + channelCount; j++) {
+      for (int r = 0; r < nranks; r++) {
+        if (kind == ORC_REDUCE_SCATTER) {
+          float v = ring_fold(&g, send, rank_at, index[r], (size_t)r * count + j);
+          store_from_f32(recv[r], dtype, j, v);
+        } else {
+          for (int q = 0; q < nranks; q++)
+            store_from_f32(recv[r], dtype, (size_t)q * count + j, load_as_f32(send[q], dtype, j));
         }
       }
     }
