@@ -41,7 +41,7 @@ PROTO_BY_NAME = {"LL": Proto.LL, "LL128": Proto.LL128, "Simple": Proto.SIMPLE, "
 EXPORTED = (
     "rar_workspace_bytes", "rar_workspace_init", "rar_allreduce", "rar_oneshot", "rar_get_status",
     "rar_strerror", "rar_set_spin_timeout_ns", "rar_debug_set_fault", "rar_describe_geometry",
-    "rar_allreduce_static", "rar_allreduce_ex",
+    "rar_allreduce_static", "rar_allreduce_ex", "rar_reduce_scatter", "rar_all_gather",
 )
 
 
@@ -88,6 +88,10 @@ def load_library():
     L.rar_allreduce_static.restype = I
     L.rar_allreduce_ex.argtypes = [P, P, I, SZ, I, I, P, I, U64, I, SZ, I, ctypes.c_uint, P, SZ, P]
     L.rar_allreduce_ex.restype = I
+    L.rar_reduce_scatter.argtypes = [P, P, I, SZ, I, I, P, I, U64, I, SZ, I, ctypes.c_uint, P, SZ, P]
+    L.rar_reduce_scatter.restype = I
+    L.rar_all_gather.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I, ctypes.c_uint, P, SZ, P]
+    L.rar_all_gather.restype = I
     _lib = L
     return L
 
@@ -170,19 +174,50 @@ def allreduce(sendbufs: Sequence, recvbufs: Sequence, ring_order: Sequence[int],
 FLAG_DIRECT = 1
 
 
+def _ring_array(ring_orders):
+    """(C array, nrings) for one ring order (a list of ranks) or one per channel."""
+    rings = [list(r) for r in ring_orders] if isinstance(ring_orders[0], (list, tuple)) else [list(ring_orders)]
+    flat = [int(v) for r in rings for v in r]
+    return (ctypes.c_int * len(flat))(*flat), len(rings)
+
+
 def allreduce_ex(sendbufs: Sequence, recvbufs: Sequence, ring_orders, mask: int, proto, workspace: Workspace,
                  buff_size: int = 0, chunk_steps: int = 4, direct: bool = False, stream=None) -> None:
     """Enqueue one ring AllReduce with one ring order (a list of ranks) or one
     per channel (a list of lists), optionally with direct all-gather writes."""
     n = len(sendbufs)
-    rings = [list(r) for r in ring_orders] if isinstance(ring_orders[0], (list, tuple)) else [list(ring_orders)]
-    flat = [v for r in rings for v in r]
-    ring_arr = (ctypes.c_int * len(flat))(*flat)
+    ring_arr, nrings = _ring_array(ring_orders)
     st = load_library().rar_allreduce_ex(_ptrs(sendbufs), _ptrs(recvbufs), n, sendbufs[0].numel(),
-                                         int(_dtype_of(sendbufs[0])), 0, ring_arr, len(rings), mask,
+                                         int(_dtype_of(sendbufs[0])), 0, ring_arr, nrings, mask,
                                          int(_proto(proto)), buff_size, chunk_steps, FLAG_DIRECT if direct else 0,
                                          workspace.ptr, workspace.nbytes, _stream_handle(stream))
     _check(st, "rar_allreduce_ex")
+
+
+def reduce_scatter(sendbufs: Sequence, recvbufs: Sequence, ring_orders, mask: int, proto, workspace: Workspace,
+                   buff_size: int = 0, chunk_steps: int = 4, stream=None) -> None:
+    """Enqueue one ring ReduceScatter (sum): sendbufs[r] holds nranks blocks of
+    recvbufs[r].numel() elements; recvbufs[r] receives block r reduced."""
+    n = len(sendbufs)
+    ring_arr, nrings = _ring_array(ring_orders)
+    st = load_library().rar_reduce_scatter(_ptrs(sendbufs), _ptrs(recvbufs), n, recvbufs[0].numel(),
+                                           int(_dtype_of(sendbufs[0])), 0, ring_arr, nrings, mask,
+                                           int(_proto(proto)), buff_size, chunk_steps, 0,
+                                           workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    _check(st, "rar_reduce_scatter")
+
+
+def all_gather(sendbufs: Sequence, recvbufs: Sequence, ring_orders, mask: int, proto, workspace: Workspace,
+               buff_size: int = 0, chunk_steps: int = 4, direct: bool = False, stream=None) -> None:
+    """Enqueue one ring AllGather: recvbufs[r] (nranks blocks) receives every
+    rank's sendbufs[b] as block b."""
+    n = len(sendbufs)
+    ring_arr, nrings = _ring_array(ring_orders)
+    st = load_library().rar_all_gather(_ptrs(sendbufs), _ptrs(recvbufs), n, sendbufs[0].numel(),
+                                       int(_dtype_of(sendbufs[0])), ring_arr, nrings, mask, int(_proto(proto)),
+                                       buff_size, chunk_steps, FLAG_DIRECT if direct else 0,
+                                       workspace.ptr, workspace.nbytes, _stream_handle(stream))
+    _check(st, "rar_all_gather")
 
 
 def allreduce_raw(send_ptrs, recv_ptrs, nranks, count, dtype, ring_order, mask, proto, buff_size, chunk_steps,

@@ -64,6 +64,10 @@ bool overlaps(const void* a, const void* b, int64_t bytes) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + (uintptr_t)bytes && y < x + (uintptr_t)bytes;
 }
+bool overlaps2(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return abytes > 0 && bbytes > 0 && x < y + (uintptr_t)bbytes && y < x + (uintptr_t)abytes;
+}
 
 // Buffers: non-null, 16-byte aligned; a receive buffer may coincide exactly
 // with its own rank's send buffer (in place) and must not overlap anything
@@ -111,6 +115,92 @@ __global__ void init_header_kernel(char* ws, int nranks, uint64_t mask, int prot
   }
 }
 
+// Buffers of the halves. ReduceScatter: send nranks blocks, recv one;
+// AllGather: send one block, recv nranks. All non-null and 16-byte aligned;
+// no receive buffer overlaps another one or another rank's send buffer. A
+// rank's own pair may overlap only in the in-place shape, where the one-block
+// buffer is the rank's own block of the other (ReduceScatter: recv == send +
+// rank*block; AllGather: send == recv + rank*block).
+rar_status check_half_buffers(int kind, const void* const* send, void* const* recv, int n, int64_t block) {
+  if (send == nullptr || recv == nullptr) return RAR_ERR_ARG;
+  const int64_t sbytes = kind == kReduceScatter ? n * block : block;
+  const int64_t rbytes = kind == kReduceScatter ? block : n * block;
+  for (int r = 0; r < n; r++) {
+    if (send[r] == nullptr || recv[r] == nullptr) return RAR_ERR_ARG;
+    if (!aligned16(send[r]) || !aligned16(recv[r])) return RAR_ERR_ALIGN;
+  }
+  for (int r = 0; r < n; r++) {
+    for (int q = 0; q < n; q++) {
+      if (q != r && overlaps2(recv[r], rbytes, recv[q], rbytes)) return RAR_ERR_ARG;
+      if (!overlaps2(recv[r], rbytes, send[q], sbytes)) continue;
+      const char* own = kind == kReduceScatter ? (const char*)send[r] + r * block : (const char*)recv[r] + r * block;
+      const void* one = kind == kReduceScatter ? (const void*)recv[r] : send[r];
+      if (q != r || own != one) return RAR_ERR_ARG;
+    }
+  }
+  return RAR_OK;
+}
+
+// One ring collective of any kind: argument checks, ring tables, launch.
+rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                    rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
+                    rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, void* workspace,
+                    size_t workspaceBytes, void* stream) {
+  if (op != RAR_SUM) return RAR_ERR_ARG;
+  if (nranks < 2 || nranks > kMaxRanks) return RAR_ERR_ARG;
+  if (count > (size_t)INT64_MAX / 4 / (size_t)nranks) return RAR_ERR_ARG;
+  if ((flags & ~(unsigned)RAR_FLAG_DIRECT) != 0) return RAR_ERR_ARG;
+  const bool direct = (flags & RAR_FLAG_DIRECT) != 0;
+  if (direct && proto != RAR_SIMPLE) return RAR_ERR_ARG;
+  // ReduceScatter carries no final value from rank to rank: nothing to write directly
+  if (direct && kind == kReduceScatter) return RAR_ERR_ARG;
+  if (kind != kAllReduce && proto != RAR_SIMPLE) return RAR_ERR_ARG;  // the halves run on Simple
+  Geometry g;
+  if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
+                    chunkSteps, kind) != 0)
+    return RAR_ERR_ARG;
+  if (nrings != 1 && nrings != g.nchan) return RAR_ERR_ARG;
+  if (ring_orders == nullptr) return RAR_ERR_ARG;
+  RingArgs a;
+  std::memset(&a, 0, sizeof a);
+  // one ring for every channel, or one per dense channel ([C12] "GRAPH 重建：N=4")
+  for (int ch = 0; ch < g.nchan; ch++) {
+    int idx[kMaxRanks];
+    const rar_status st = setup_ring(nranks, ring_orders + (nrings == 1 ? 0 : (size_t)ch * nranks), idx);
+    if (st != RAR_OK) return st;
+    for (int r = 0; r < nranks; r++) {
+      a.ring_index[ch * kMaxRanks + r] = (uint8_t)idx[r];
+      a.ring_rank[ch * kMaxRanks + idx[r]] = (uint8_t)r;
+    }
+  }
+  const int64_t block = (int64_t)count * g.elem_bytes;
+  rar_status st = kind == kAllReduce ? check_buffers(sendbufs, recvbufs, nranks, block, true)
+                                     : check_half_buffers(kind, sendbufs, recvbufs, nranks, block);
+  if (st != RAR_OK) return st;
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
+  if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, g.nchan, g.buff_size)) return RAR_ERR_WORKSPACE;
+  // An empty call enqueues nothing and advances no step counter ([OS89],
+  // review of the empty-input case).
+  if (count == 0) return RAR_OK;
+  for (int r = 0; r < nranks; r++) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  a.geo = g;
+  a.mask = channelMask;
+  a.ws = (char*)workspace;
+  a.conn_offset = kHeaderBytes;
+  a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
+  a.timeout_ns = spin_timeout_ns();
+  a.fault = g_fault.load(std::memory_order_relaxed);
+  a.direct = direct ? 1 : 0;
+  const int grid = nranks * g.nchan;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = (g.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr) : launch_ring_line(a, grid, s, nullptr);
+  return from_cuda(e);
+}
+
 }  // namespace
 }  // namespace rar
 
@@ -143,50 +233,24 @@ rar_status rar_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, 
                             rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
                             rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, void* workspace,
                             size_t workspaceBytes, void* stream) {
-  if (op != RAR_SUM) return RAR_ERR_ARG;
-  if (count > (size_t)INT64_MAX / 4) return RAR_ERR_ARG;
-  if ((flags & ~(unsigned)RAR_FLAG_DIRECT) != 0) return RAR_ERR_ARG;
-  const bool direct = (flags & RAR_FLAG_DIRECT) != 0;
-  if (direct && proto != RAR_SIMPLE) return RAR_ERR_ARG;
-  Geometry g;
-  if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
-                    chunkSteps) != 0)
-    return RAR_ERR_ARG;
-  if (nrings != 1 && nrings != g.nchan) return RAR_ERR_ARG;
-  if (ring_orders == nullptr) return RAR_ERR_ARG;
-  RingArgs a;
-  std::memset(&a, 0, sizeof a);
-  // one ring for every channel, or one per dense channel ([C12] "GRAPH 重建：N=4")
-  for (int ch = 0; ch < g.nchan; ch++) {
-    int idx[kMaxRanks];
-    const rar_status st = setup_ring(nranks, ring_orders + (nrings == 1 ? 0 : (size_t)ch * nranks), idx);
-    if (st != RAR_OK) return st;
-    for (int r = 0; r < nranks; r++) a.ring_index[ch * kMaxRanks + r] = (uint8_t)idx[r];
-  }
-  rar_status st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * g.elem_bytes, true);
-  if (st != RAR_OK) return st;
-  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
-  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
-  if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, g.nchan, g.buff_size)) return RAR_ERR_WORKSPACE;
-  // An empty call enqueues nothing and advances no step counter ([OS89],
-  // review of the empty-input case).
-  if (count == 0) return RAR_OK;
-  for (int r = 0; r < nranks; r++) {
-    a.send[r] = sendbufs[r];
-    a.recv[r] = recvbufs[r];
-  }
-  a.geo = g;
-  a.mask = channelMask;
-  a.ws = (char*)workspace;
-  a.conn_offset = kHeaderBytes;
-  a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
-  a.timeout_ns = spin_timeout_ns();
-  a.fault = g_fault.load(std::memory_order_relaxed);
-  a.direct = direct ? 1 : 0;
-  const int grid = nranks * g.nchan;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = (g.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr) : launch_ring_line(a, grid, s, nullptr);
-  return from_cuda(e);
+  return run_ring(kAllReduce, sendbufs, recvbufs, nranks, count, dtype, op, ring_orders, nrings, channelMask, proto,
+                  buffSize, chunkSteps, flags, workspace, workspaceBytes, stream);
+}
+
+rar_status rar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t recvcount,
+                              rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings,
+                              uint64_t channelMask, rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags,
+                              void* workspace, size_t workspaceBytes, void* stream) {
+  return run_ring(kReduceScatter, sendbufs, recvbufs, nranks, recvcount, dtype, op, ring_orders, nrings, channelMask,
+                  proto, buffSize, chunkSteps, flags, workspace, workspaceBytes, stream);
+}
+
+rar_status rar_all_gather(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t sendcount,
+                          rar_dtype dtype, const int* ring_orders, int nrings, uint64_t channelMask, rar_proto proto,
+                          size_t buffSize, int chunkSteps, unsigned flags, void* workspace, size_t workspaceBytes,
+                          void* stream) {
+  return run_ring(kAllGather, sendbufs, recvbufs, nranks, sendcount, dtype, RAR_SUM, ring_orders, nrings,
+                  channelMask, proto, buffSize, chunkSteps, flags, workspace, workspaceBytes, stream);
 }
 
 rar_status rar_allreduce(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,

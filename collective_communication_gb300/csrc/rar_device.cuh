@@ -73,6 +73,7 @@ struct RingArgs {
   const void* send[kMaxRanks];
   void* recv[kMaxRanks];
   uint8_t ring_index[kMaxChannels * kMaxRanks];  // [dense channel * kMaxRanks + user rank] -> ring index
+  uint8_t ring_rank[kMaxChannels * kMaxRanks];   // [dense channel * kMaxRanks + ring index] -> user rank
   int direct;                  // Simple: all-gather hops write the next rank's output directly
   Geometry geo;
   uint64_t mask;
@@ -300,11 +301,28 @@ __device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* den
 __device__ __forceinline__ int ring_index_of(const RingArgs& a, int dense, int rank) {
   return a.ring_index[dense * kMaxRanks + rank];
 }
+__device__ __forceinline__ int rank_at_index(const RingArgs& a, int dense, int ring_idx) {
+  return a.ring_rank[dense * kMaxRanks + ring_idx];
+}
 __device__ __forceinline__ int next_rank_of(const RingArgs& a, int dense, int ring_idx) {
-  const int want = (ring_idx + 1) % a.geo.nranks;
-  for (int r = 0; r < a.geo.nranks; r++)
-    if (a.ring_index[dense * kMaxRanks + r] == want) return r;
-  return 0;
+  return rank_at_index(a, dense, (ring_idx + 1) % a.geo.nranks);
+}
+
+// Element offsets of the current slice in the rank's input and output.
+// AllReduce: the same offset in both. The halves: a ReduceScatter input and
+// an AllGather output hold nranks blocks of geo.count elements, block b
+// belonging to user rank b; a slice of the chunk with ring index c lies in
+// the block of the user rank at ring index c. The other buffer holds one block.
+__device__ __forceinline__ void slice_offsets(const RingArgs& a, int dense, const SliceCursor& c, int64_t* in_off,
+                                              int64_t* out_off) {
+  const Geometry& g = a.geo;
+  if (g.kind == kAllReduce) {
+    *in_off = *out_off = c.offset;
+    return;
+  }
+  const int64_t blk = (int64_t)rank_at_index(a, dense, c.chunk) * g.count;
+  *in_off = c.offset + (g.kind == kReduceScatter ? blk : 0);
+  *out_off = c.offset + (g.kind == kAllGather ? blk : 0);
 }
 
 // Entry check shared by the ring kernels (thread 0): the workspace must be

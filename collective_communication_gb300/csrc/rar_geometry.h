@@ -24,13 +24,19 @@ constexpr int kMaxChannels = 64;
 enum Proto : int { kLL = 0, kLL128 = 1, kSimple = 2 };
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
+// Collectives built on the ring: AllReduce, and its two halves on their own
+// ([C12] "Ring AllReduce 不只是“绕一圈”": AllReduce = ReduceScatter + AllGather).
+enum Kind : int { kAllReduce = 0, kReduceScatter = 1, kAllGather = 2 };
+
 // Rows of the per-rank schedule ([C12] "源码步骤一" .. "源码步骤五").
 enum Prim : int {
   kSend = 0,                // raw local input -> next
   kRecvReduceSend = 1,      // prev + local -> next
   kRecvReduceCopySend = 2,  // prev + local -> output and next (owner row)
   kRecvCopySend = 3,        // prev -> output and next
-  kRecv = 4                 // prev -> output
+  kRecv = 4,                // prev -> output
+  kRecvReduceCopy = 5,      // prev + local -> output (ReduceScatter's owner row)
+  kCopySend = 6             // local -> output and next (AllGather's first row)
 };
 
 RAR_HD int64_t div_up(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -38,22 +44,37 @@ RAR_HD int64_t align_up(int64_t a, int64_t b) { return div_up(a, b) * b; }
 RAR_HD int64_t imin(int64_t a, int64_t b) { return a < b ? a : b; }
 RAR_HD int64_t imax(int64_t a, int64_t b) { return a > b ? a : b; }
 
-RAR_HD int prim_of_row(int n, int s) {
+RAR_HD int rows_per_loop(int kind, int n) { return kind == kAllReduce ? 2 * n - 1 : n; }
+
+RAR_HD int prim_of_row(int kind, int n, int s) {
+  if (kind == kReduceScatter) return s == 0 ? kSend : s < n - 1 ? kRecvReduceSend : kRecvReduceCopy;
+  if (kind == kAllGather) return s == 0 ? kCopySend : s < n - 1 ? kRecvCopySend : kRecv;
   return s == 0 ? kSend
        : s < n - 1 ? kRecvReduceSend
        : s == n - 1 ? kRecvReduceCopySend
        : s < 2 * n - 2 ? kRecvCopySend
        : kRecv;
 }
-// chunk of row s for ring index i: every formula of the page, (i + n - j) with
-// its own loop counter j, is (i - s - 1) mod n for the row number s.
-RAR_HD int chunk_of_row(int n, int i, int s) { return ((i - s - 1) % n + 2 * n) % n; }
-RAR_HD bool row_recvs(int prim) { return prim != kSend; }
-RAR_HD bool row_sends(int prim) { return prim != kRecv; }
+// Chunk (ring index of its owner) of row s for ring index i: every formula of
+// the page, (i + n - j) with its own loop counter j, is (i - s - 1) mod n for
+// the row number s. The AllGather half starts at the rank's own chunk, so its
+// row s carries chunk (i - s) mod n.
+RAR_HD int chunk_of_row(int kind, int n, int i, int s) {
+  const int d = kind == kAllGather ? s : s + 1;
+  return ((i - d) % n + 2 * n) % n;
+}
+RAR_HD bool row_recvs(int prim) { return prim != kSend && prim != kCopySend; }
+RAR_HD bool row_sends(int prim) { return prim != kRecv && prim != kRecvReduceCopy; }
+RAR_HD bool row_reads_input(int prim) {
+  return prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend || prim == kRecvReduceCopy ||
+         prim == kCopySend;
+}
 // Partial sums (binary32) cross the reduce-scatter hops; final values (T)
 // cross the all-gather hops.
 RAR_HD bool row_sends_partial(int prim) { return prim == kSend || prim == kRecvReduceSend; }
-RAR_HD bool row_recvs_partial(int prim) { return prim == kRecvReduceSend || prim == kRecvReduceCopySend; }
+RAR_HD bool row_recvs_partial(int prim) {
+  return prim == kRecvReduceSend || prim == kRecvReduceCopySend || prim == kRecvReduceCopy;
+}
 
 RAR_HD int64_t default_buff_size(int proto) {
   return proto == kSimple ? (int64_t)4 << 20   // "default" row of [C23] "Simple Buffer Sweep"
@@ -63,8 +84,9 @@ RAR_HD int64_t default_buff_size(int proto) {
 
 // Resolved per-call geometry.
 struct Geometry {
+  int kind;             // kAllReduce, kReduceScatter or kAllGather
   int proto, dtype, nranks, nchan;
-  int64_t count;        // elements per rank
+  int64_t count;        // elements per rank (AllReduce) or per rank block (ReduceScatter, AllGather)
   int elem_bytes;       // sizeof(T)
   int align_elems;      // 16 / sizeof(T)
   int64_t buff_size;    // FIFO bytes per connection
@@ -78,7 +100,9 @@ struct Geometry {
 
 // Returns 0 on success, 1 for a bad argument.
 RAR_HD int make_geometry(Geometry* g, int proto, int dtype, int nranks, uint64_t mask, int64_t count,
-                         int64_t buff_size, int chunk_steps) {
+                         int64_t buff_size, int chunk_steps, int kind = kAllReduce) {
+  if (kind != kAllReduce && kind != kReduceScatter && kind != kAllGather) return 1;
+  g->kind = kind;
   if (nranks < 2 || nranks > kMaxRanks) return 1;
   if (dtype != kF32 && dtype != kBF16) return 1;
   if (proto != kLL && proto != kLL128 && proto != kSimple) return 1;
@@ -128,12 +152,18 @@ RAR_HD void channel_range(const Geometry& g, int n, int64_t* grid_offset, int64_
   *channel_count = off >= g.count ? 0 : imin(g.per_channel, g.count - off);
 }
 
-RAR_HD int64_t loop_count(const Geometry& g) { return (int64_t)g.nranks * g.chunk_elems; }
+// Elements of the channel range one loop covers: AllReduce splits a loop into
+// nranks chunks of the rank's buffer; the two halves move one chunk of every
+// rank block per loop (the block is the chunk).
+RAR_HD int64_t loop_count(const Geometry& g) {
+  return g.kind == kAllReduce ? (int64_t)g.nranks * g.chunk_elems : g.chunk_elems;
+}
 
 // Chunk size of a loop whose remainder is rem: full chunks, except in the
 // short last loop, split over the ranks and aligned up to 16/sizeof(T)
-// ([C12] "runRing 的数据切分").
+// ([C12] "runRing 的数据切分"); for the halves, the remainder itself.
 RAR_HD int64_t loop_chunk_count(const Geometry& g, int64_t rem) {
+  if (g.kind != kAllReduce) return imin(rem, g.chunk_elems);
   return rem < loop_count(g) ? align_up(div_up(rem, g.nranks), g.align_elems) : g.chunk_elems;
 }
 
@@ -161,18 +191,27 @@ struct SliceCursor {
   bool valid;
   // current slice
   int prim;
-  int64_t offset;  // user element offset
+  int chunk;       // ring index of the chunk's owner
+  int64_t offset;  // AllReduce: user element offset; halves: offset inside the rank block
   int64_t nelem;
 };
 
 RAR_HD void cursor_fill(const Geometry& g, SliceCursor& c) {
   int n = g.nranks;
-  int ch = chunk_of_row(n, c.ring_index, c.s);
-  int64_t ne = chunk_nelem(c.chunk_count, c.rem, ch);
+  int ch = chunk_of_row(g.kind, n, c.ring_index, c.s);
+  int64_t ne, base;
+  if (g.kind == kAllReduce) {
+    ne = chunk_nelem(c.chunk_count, c.rem, ch);
+    base = c.grid_offset + c.elem_offset + c.chunk_count * ch;
+  } else {
+    ne = c.chunk_count;  // the same range of every rank block
+    base = c.grid_offset + c.elem_offset;
+  }
   int64_t ss = slice_size(g, ne);
   int64_t so = ss * c.k;
-  c.prim = prim_of_row(n, c.s);
-  c.offset = c.grid_offset + c.elem_offset + c.chunk_count * ch + so;
+  c.prim = prim_of_row(g.kind, n, c.s);
+  c.chunk = ch;
+  c.offset = base + so;
   c.nelem = ne > so ? imin(ss, ne - so) : 0;  // empty slices still wait and post
 }
 
@@ -193,7 +232,7 @@ RAR_HD void cursor_begin(const Geometry& g, int dense_channel, int ring_index, S
 RAR_HD void cursor_next(const Geometry& g, SliceCursor& c) {
   if (++c.k < g.spc) { cursor_fill(g, c); return; }
   c.k = 0;
-  if (++c.s < 2 * g.nranks - 1) { cursor_fill(g, c); return; }
+  if (++c.s < rows_per_loop(g.kind, g.nranks)) { cursor_fill(g, c); return; }
   c.s = 0;
   c.elem_offset += loop_count(g);
   if (c.elem_offset >= c.channel_count) { c.valid = false; return; }

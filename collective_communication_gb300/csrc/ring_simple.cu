@@ -143,19 +143,24 @@ __device__ __forceinline__ uint16_t load_final_scalar<uint16_t>(const char* p) {
 // the next rank's output (g_next) instead of the send FIFO, and a received
 // final is already in this rank's own output (staged from there, not from the
 // FIFO), so it is neither stored again nor, on the last row, moved at all.
+// covered == 0 (a slice whose user pointers are not 16-byte aligned, which
+// only a ragged block of the halves gives): every element takes the scalar path.
 template <typename T, int PRIM, bool DIRECT>
 __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv, const T* __restrict__ g_in,
                                              T* __restrict__ g_out, T* __restrict__ g_next, const char* rslot,
                                              char* sslot, int64_t e0, int ne, int covered, int ct, int nct,
                                              uint64_t out_policy) {
   constexpr int P = ElemTraits<T>::kPack;
-  constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
+  constexpr bool kReduce = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kFinalOfSum = PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kIn = PRIM == kSend || kReduce || PRIM == kCopySend;
+  constexpr bool kRecvPartial = kReduce;
   constexpr bool kRecvFinal = (PRIM == kRecvCopySend || PRIM == kRecv) && !(DIRECT && PRIM == kRecv);
   constexpr bool kSendPartial = PRIM == kSend || PRIM == kRecvReduceSend;
-  constexpr bool kSendFinal = (PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend) && !DIRECT;
-  constexpr bool kSendNext = (PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend) && DIRECT;
-  constexpr bool kOut = PRIM == kRecvReduceCopySend || ((PRIM == kRecvCopySend || PRIM == kRecv) && !DIRECT);
+  constexpr bool kForward = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kCopySend;
+  constexpr bool kSendFinal = kForward && !DIRECT;
+  constexpr bool kSendNext = kForward && DIRECT;
+  constexpr bool kOut = kFinalOfSum || PRIM == kCopySend || ((PRIM == kRecvCopySend || PRIM == kRecv) && !DIRECT);
   if constexpr (DIRECT && PRIM == kRecv) return;  // the data is already in place
   constexpr int U = 4;
   const int npacks = covered / P;
@@ -166,9 +171,9 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
       if (j < npacks) {
         const int64_t e = e0 + (int64_t)j * P;
         float x[P], v[P];
-        uint4 fin;
-        if (kIn) {
-          const uint4 w = *reinterpret_cast<const uint4*>(s_in + j * 16);
+        uint4 fin, w = make_uint4(0u, 0u, 0u, 0u);
+        if (kIn) w = *reinterpret_cast<const uint4*>(s_in + j * 16);
+        if (kIn && PRIM != kCopySend) {
           if constexpr (P == 4) {
             x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
             x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
@@ -190,7 +195,8 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
           for (int k = 0; k < P; k++) v[k] = x[k];
         }
         if (kRecvFinal) fin = *reinterpret_cast<const uint4*>(s_rcv + j * 16);
-        if (PRIM == kRecvReduceCopySend) fin = to_final_pack<T>(v);
+        if (kFinalOfSum) fin = to_final_pack<T>(v);
+        if (PRIM == kCopySend) fin = w;  // the input is already a final value
         if (kSendPartial) store_partial_pack<P>(sslot + e * 4, v);
         if (kSendFinal) st_v4(sslot + e * (int64_t)sizeof(T), fin);
         if (kSendNext) st_v4(g_next + e, fin);  // read back by the next rank: default L2 policy
@@ -203,7 +209,8 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
     const int64_t e = e0 + k;
     float xv = 0.f, pv = 0.f;
     T fv{};
-    if (kIn) xv = load_input_scalar<T>(g_in + e);
+    if (kIn && PRIM != kCopySend) xv = load_input_scalar<T>(g_in + e);
+    if (PRIM == kCopySend) fv = load_final_scalar<T>(reinterpret_cast<const char*>(g_in + e));
     if (kRecvPartial) pv = __uint_as_float(ld_cg_u32(rslot + e * 4));
     if (kRecvFinal)
       fv = DIRECT ? load_final_scalar<T>(reinterpret_cast<const char*>(g_out + e))
@@ -212,7 +219,7 @@ __device__ __forceinline__ void tile_compute(const char* s_in, const char* s_rcv
       *reinterpret_cast<float*>(sslot + e * 4) = xv;
     } else if (PRIM == kRecvReduceSend) {
       *reinterpret_cast<float*>(sslot + e * 4) = __fadd_rn(pv, xv);
-    } else if (PRIM == kRecvReduceCopySend) {
+    } else if (kFinalOfSum) {
       fv = final_scalar<T>(__fadd_rn(pv, xv));
     }
     if (kOut) g_out[e] = fv;
@@ -241,6 +248,14 @@ __device__ __forceinline__ void tile_compute_prim(int prim, const char* s_in, co
       tile_compute<T, kRecvCopySend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct,
                                              nct, pol);
       break;
+    case kRecvReduceCopy:
+      tile_compute<T, kRecvReduceCopy, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct,
+                                               nct, pol);
+      break;
+    case kCopySend:
+      tile_compute<T, kCopySend, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct,
+                                         pol);
+      break;
     default:
       tile_compute<T, kRecv, DIRECT>(s_in, s_rcv, g_in, g_out, g_next, rslot, sslot, e0, ne, covered, ct, nct, pol);
       break;
@@ -260,7 +275,7 @@ __device__ __forceinline__ void tile_compute_any(bool direct, int prim, const ch
 // Rows of the direct mode: all-gather sends go to the next rank's output,
 // all-gather receives find their data in this rank's own output.
 __device__ __forceinline__ bool direct_send_row(bool direct, int prim) {
-  return direct && (prim == kRecvReduceCopySend || prim == kRecvCopySend);
+  return direct && (prim == kRecvReduceCopySend || prim == kRecvCopySend || prim == kCopySend);
 }
 __device__ __forceinline__ bool direct_recv_row(bool direct, int prim) {
   return direct && (prim == kRecvCopySend || prim == kRecv);
@@ -281,6 +296,13 @@ __host__ __device__ constexpr int max_stages() {
 }
 
 __device__ __forceinline__ bool recv_is_partial(int prim) { return row_recvs_partial(prim); }
+
+// A slice's user pointers all 16-byte aligned: its packs may be bulk-copied
+// and stored 16 bytes at a time.
+template <typename T>
+__device__ __forceinline__ bool user_vec_ok(const T* in, const T* out, const T* next) {
+  return (((uintptr_t)in | (uintptr_t)out | (uintptr_t)next) & 15u) == 0;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __grid_constant__ RingArgs a,
@@ -384,7 +406,10 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         break;
       }
       const int prim = c.prim;
-      const bool has_in = prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend;
+      int64_t in_off, out_off;
+      slice_offsets(a, dense, c, &in_off, &out_off);
+      const bool vec = user_vec_ok(in + in_off, out + out_off, direct ? next_out + out_off : nullptr);
+      const bool has_in = row_reads_input(prim);
       const bool has_rcv = row_recvs(prim);
       // direct mode: a forwarded final is staged from this rank's own output,
       // the last row moves nothing
@@ -402,15 +427,15 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         }
         const int64_t e0 = (int64_t)k * kTileElems;
         const int ne = (int)imin(kTileElems, c.nelem - e0);
-        const int covered = ne / P * P;
+        const int covered = vec ? ne / P * P : 0;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
         const uint32_t b_rcv = rcv_bytes ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
         char* s_in = smem + (int64_t)st * SB;
         char* s_rcv = s_in + kTileElems * (int)sizeof(T);
         mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
-        if (b_in) tma_load_1d(s_in, in + c.offset + e0, b_in, &bar_full[st], pol);
+        if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         if (b_rcv)
-          tma_load_1d(s_rcv, rcv_own_out ? reinterpret_cast<const char*>(out + c.offset + e0) : rslot + e0 * rcv_eb,
+          tma_load_1d(s_rcv, rcv_own_out ? reinterpret_cast<const char*>(out + out_off + e0) : rslot + e0 * rcv_eb,
                       b_rcv, &bar_full[st], pol);
         gt++;
       }
@@ -468,6 +493,9 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       }
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
+      int64_t in_off, out_off;
+      slice_offsets(a, dense, c, &in_off, &out_off);
+      const bool vec = user_vec_ok(in + in_off, out + out_off, direct ? next_out + out_off : nullptr);
       const int ntiles = (int)div_up(c.nelem, kTileElems);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
@@ -480,9 +508,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         const int ne = (int)imin(kTileElems, c.nelem - e0);
         const char* s_in = smem + (int64_t)st * SB;
         const char* s_rcv = s_in + kTileElems * (int)sizeof(T);
-        tile_compute_any<T>(direct, c.prim, s_in, s_rcv, in + c.offset, out + c.offset, next_out + c.offset, rslot,
-                            sslot, e0, ne, ne / P * P,
-                            ct, kComputeThreads, out_pol);
+        tile_compute_any<T>(direct, c.prim, s_in, s_rcv, in + in_off, out + out_off, next_out + out_off, rslot,
+                            sslot, e0, ne, vec ? ne / P * P : 0, ct, kComputeThreads, out_pol);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);
       }

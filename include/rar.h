@@ -167,6 +167,53 @@ RAR_API rar_status rar_allreduce_ex(const void* const* sendbufs, void* const* re
                                     void* workspace, size_t workspaceBytes, void* stream);
 
 /*
+ * ReduceScatter (sum) and AllGather on the ring: the two halves of the ring
+ * AllReduce ([C12] "Ring AllReduce 不只是“绕一圈”": AllReduce is ReduceScatter
+ * followed by AllGather; "源码步骤三": the owner row is the last recv+reduce of
+ * the first and the first send of the second) run as collectives of their own,
+ * each with nranks rows per chunk loop instead of 2*nranks-1:
+ *   ReduceScatter  send, recvReduceSend x (nranks-2), recvReduceCopy
+ *   AllGather      copySend, recvCopySend x (nranks-2), recv
+ * A block is `count` elements (recvcount, sendcount). The channels split the
+ * block range exactly as rar_allreduce splits a rank's buffer; a chunk loop
+ * moves one chunk of every block: the chunk with ring index c is that range of
+ * the block of the user rank at ring index c on the channel's ring.
+ *
+ * rar_reduce_scatter: sendbufs[r] holds nranks blocks (nranks*recvcount
+ *   elements), block b for user rank b; recvbufs[r] receives block r reduced
+ *   over all ranks, in binary32, in ring order starting after r and ending with
+ *   r's own input (the AllReduce fold of a chunk owned by r), rounded once for
+ *   bf16. Partial sums cross the hops as binary32.
+ * rar_all_gather: sendbufs[r] holds one block (sendcount elements);
+ *   recvbufs[r] (nranks*sendcount elements) receives block b = sendbufs[b],
+ *   bit for bit.
+ * Buffers: device pointers, 16-byte aligned; a receive buffer may not overlap
+ *   another receive buffer or another rank's send buffer; a rank's own pair
+ *   may overlap only in the in-place shape (ReduceScatter: recvbufs[r] ==
+ *   sendbufs[r] + r*recvcount elements; AllGather: sendbufs[r] == recvbufs[r] +
+ *   r*sendcount elements); anything else is RAR_ERR_ARG. A block of a count
+ *   that is not a multiple of 16/sizeof(T) is moved element by element
+ *   (correct, slower).
+ * proto: RAR_SIMPLE (else RAR_ERR_ARG). flags: 0, or RAR_FLAG_DIRECT for
+ *   rar_all_gather only (its hops write the next rank's receive buffer
+ *   directly, as in rar_allreduce_ex); RAR_FLAG_DIRECT with rar_reduce_scatter
+ *   is RAR_ERR_ARG.
+ * ring_orders, nrings, channelMask, buffSize, chunkSteps, workspace, stream
+ * and every error as for rar_allreduce_ex; the workspace is the one
+ * rar_workspace_init prepares for (nranks, channelMask, proto, buffSize), and
+ * its step counters carry over between calls of any of the three collectives.
+ */
+RAR_API rar_status rar_reduce_scatter(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                                      size_t recvcount, rar_dtype dtype, rar_redop op,
+                                      const int* ring_orders, int nrings, uint64_t channelMask,
+                                      rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags,
+                                      void* workspace, size_t workspaceBytes, void* stream);
+RAR_API rar_status rar_all_gather(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                                  size_t sendcount, rar_dtype dtype, const int* ring_orders, int nrings,
+                                  uint64_t channelMask, rar_proto proto, size_t buffSize, int chunkSteps,
+                                  unsigned flags, void* workspace, size_t workspaceBytes, void* stream);
+
+/*
  * One-shot AllReduce (sum) over nranks virtual ranks ([OS89], the single
  * kernel form; [NOTES] "5 Symmetric Memory": a rank reads its peers' buffers
  * by pointer): every rank reads all peers' inputs and reduces them itself,

@@ -151,3 +151,66 @@ def test_allreduce_ex_argument_errors(lib):
     assert call_ex(flags=1, count=0) == S.OK
     assert call_ex(flags=2) == S.ERR_ARG
     assert call_ex(wsb=16) == S.ERR_WORKSPACE
+
+
+def call_half(kind, n=4, count=1024, mask=0b11, proto=B.Proto.SIMPLE, flags=0, send=None, recv=None, ws=FAKE,
+              wsb=1 << 30, dtype=0, op=0, rings=None):
+    rings = [list(range(n))] if rings is None else rings
+    flat = [v for r in rings for v in r]
+    send = [FAKE + (i << 28) for i in range(n)] if send is None else send
+    recv = [FAKE + (1 << 35) + (i << 28) for i in range(n)] if recv is None else recv
+    L = B.load_library()
+    sp = (ctypes.c_void_p * n)(*send)
+    rp = (ctypes.c_void_p * n)(*recv)
+    rg = (ctypes.c_int * len(flat))(*flat)
+    if kind == "rs":
+        return L.rar_reduce_scatter(sp, rp, n, count, dtype, op, rg, len(rings), mask, int(proto), 65536, 4, flags,
+                                    ws, wsb, None)
+    return L.rar_all_gather(sp, rp, n, count, dtype, rg, len(rings), mask, int(proto), 65536, 4, flags, ws, wsb,
+                            None)
+
+
+@pytest.mark.parametrize("kind", ["rs", "ag"])
+def test_halves_argument_errors(lib, kind):
+    S = B.Status
+    assert call_half(kind, count=0) == S.OK  # empty: nothing enqueued
+    assert call_half(kind, proto=B.Proto.LL) == S.ERR_ARG  # the halves run on Simple
+    assert call_half(kind, proto=B.Proto.LL128) == S.ERR_ARG
+    assert call_half(kind, n=1, rings=[[0]]) == S.ERR_ARG
+    assert call_half(kind, rings=[[0, 1, 1, 3]]) == S.ERR_RING
+    assert call_half(kind, dtype=7) == S.ERR_ARG
+    assert call_half(kind, flags=2) == S.ERR_ARG
+    assert call_half(kind, wsb=16) == S.ERR_WORKSPACE
+    assert call_half(kind, ws=FAKE + 8) == S.ERR_ALIGN
+    assert call_half(kind, send=[FAKE + 4] + [FAKE + (i << 28) for i in range(1, 4)]) == S.ERR_ALIGN
+    assert call_half(kind, count=1 << 62) == S.ERR_ARG  # nranks blocks would overflow
+    if kind == "rs":
+        assert call_half(kind, op=1) == S.ERR_ARG
+        assert call_half(kind, flags=1) == S.ERR_ARG  # no final value crosses a ReduceScatter hop
+    else:
+        assert call_half(kind, flags=1, count=0) == S.OK
+
+
+@pytest.mark.parametrize("kind", ["rs", "ag"])
+def test_halves_buffer_overlap_rules(lib, kind):
+    S = B.Status
+    n, count = 4, 1024
+    blk = count * 4
+    base = [FAKE + (i << 28) for i in range(n)]
+    other = [FAKE + (1 << 35) + (i << 28) for i in range(n)]
+    # in place: the one-block buffer is the rank's own block of the n-block one
+    inplace = [b + r * blk for r, b in enumerate(base)]
+    if kind == "rs":
+        assert call_half(kind, send=base, recv=inplace, count=0) == S.OK
+        assert call_half(kind, send=base, recv=inplace, wsb=16) == S.ERR_WORKSPACE  # passed the buffer checks
+        # another rank's block, or rank r's recv inside another rank's input
+        wrong = [b + ((r + 1) % n) * blk for r, b in enumerate(base)]
+        assert call_half(kind, send=base, recv=wrong) == S.ERR_ARG
+        assert call_half(kind, send=base, recv=[base[1]] + other[1:]) == S.ERR_ARG
+    else:
+        assert call_half(kind, send=inplace, recv=base, wsb=16) == S.ERR_WORKSPACE
+        wrong = [b + ((r + 1) % n) * blk for r, b in enumerate(base)]
+        assert call_half(kind, send=wrong, recv=base) == S.ERR_ARG
+        assert call_half(kind, send=[base[1]] + other[1:], recv=base) == S.ERR_ARG
+    # two receive buffers overlapping
+    assert call_half(kind, send=other, recv=[base[0], base[0] + 16] + base[2:]) == S.ERR_ARG
