@@ -154,7 +154,6 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
   if (direct && proto != RAR_SIMPLE) return RAR_ERR_ARG;
   // ReduceScatter carries no final value from rank to rank: nothing to write directly
   if (direct && kind == kReduceScatter) return RAR_ERR_ARG;
-  if (kind != kAllReduce && proto != RAR_SIMPLE) return RAR_ERR_ARG;  // the halves run on Simple
   Geometry g;
   if (make_geometry(&g, (int)proto, (int)dtype, nranks, channelMask, (int64_t)count, (int64_t)buffSize,
                     chunkSteps, kind) != 0)
@@ -174,6 +173,9 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
     }
   }
   const int64_t block = (int64_t)count * g.elem_bytes;
+  // LL and LL128 move user data in 8- and 16-byte pieces: the halves' blocks
+  // must start on 16-byte boundaries (Simple moves a ragged block elementwise)
+  if (kind != kAllReduce && proto != RAR_SIMPLE && block % 16 != 0) return RAR_ERR_ALIGN;
   rar_status st = kind == kAllReduce ? check_buffers(sendbufs, recvbufs, nranks, block, true)
                                      : check_half_buffers(kind, sendbufs, recvbufs, nranks, block);
   if (st != RAR_OK) return st;

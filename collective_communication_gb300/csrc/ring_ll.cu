@@ -1,5 +1,6 @@
-// ring_ll.cu -- ring AllReduce, LL and LL128 protocols, all N virtual ranks in
-// one launch (one block per (rank, channel)).
+// ring_ll.cu -- ring AllReduce (and its ReduceScatter and AllGather halves),
+// LL and LL128 protocols, all N virtual ranks in one launch (one block per
+// (rank, channel)).
 //
 // Pages cited (by title, then section):
 //   [C23] "NCCL 专家课程 23：Device Kernel、Primitives、Step/Credit 与 LL Flag"
@@ -108,6 +109,29 @@ __device__ __forceinline__ void store_out_n(T* p, int n, int kmax, uint4 w) {
 
 __device__ __forceinline__ uint32_t round_bf16_pair(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
+// The first n (<= kmax) elements of T at p as raw bits, little-endian, zeros
+// past n; kmax * sizeof(T) is 16 or 8 bytes.
+template <typename T>
+__device__ __forceinline__ uint4 load_raw_n(const T* p, int n, int kmax) {
+  const int bytes = kmax * (int)sizeof(T);
+  if (n == kmax && bytes == 16) return ld_stream_v4(p);
+  if (n == kmax && bytes == 8) {
+    const uint2 u = ld_stream_v2(p);
+    return make_uint4(u.x, u.y, 0u, 0u);
+  }
+  uint32_t wd[4] = {0u, 0u, 0u, 0u};
+  for (int j = 0; j < n; j++) {
+    if constexpr (sizeof(T) == 4) {
+      wd[j] = ld_cg_u32(p + j);
+    } else {
+      uint16_t h;
+      asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(p + j) : "memory");
+      wd[j >> 1] |= (uint32_t)h << ((j & 1) * 16);
+    }
+  }
+  return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
 // ---------------------------------------------------------------------------
 // LL
 // ---------------------------------------------------------------------------
@@ -133,12 +157,13 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
   constexpr int K = LLUnit<T>::kElems;
   constexpr int PL = LLUnit<T>::kPartLines;
   constexpr int UL = 1;
-  constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kIn = PRIM == kSend || kRecvPartial || PRIM == kCopySend;
   constexpr bool kRecvFinal = PRIM == kRecvCopySend || PRIM == kRecv;
   constexpr bool kSendPartial = PRIM == kSend || PRIM == kRecvReduceSend;
-  constexpr bool kSendFinal = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend;
-  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
+  constexpr bool kSendFinal = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kCopySend;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv ||
+                        PRIM == kRecvReduceCopy || PRIM == kCopySend;
   constexpr int RL = kRecvPartial ? PL : 1;
 
   const int64_t nunits = div_up(nelem, K);
@@ -183,7 +208,8 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
         }
 #pragma unroll
         for (int j = 0; j < K; j++) v[j] = __fadd_rn(v[j], x[u][j]);
-      } else if (PRIM == kSend) {
+      } else if (PRIM == kSend || PRIM == kCopySend) {
+        // copySend: a bf16 input widened and rounded back is the same value
 #pragma unroll
         for (int j = 0; j < K; j++) v[j] = x[u][j];
       }
@@ -236,14 +262,16 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
                                             uint64_t info) {
   constexpr int NW = NT / 32;
   constexpr int UG = 1;
-  constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kHasRecv = PRIM != kSend;
-  constexpr bool kHasSend = PRIM != kRecv;
-  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
-  // payload element bytes of this row (both sides)
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kIn = PRIM == kSend || kRecvPartial;  // copySend loads its input raw
+  constexpr bool kHasRecv = PRIM != kSend && PRIM != kCopySend;
+  constexpr bool kHasSend = PRIM != kRecv && PRIM != kRecvReduceCopy;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv ||
+                        PRIM == kRecvReduceCopy || PRIM == kCopySend;
+  // payload element bytes of this row (the received side for recvReduceCopy)
   constexpr int EB = (PRIM == kSend || PRIM == kRecvReduceSend) ? 4
                    : (PRIM == kRecvReduceCopySend) ? 4  // f32 only here
+                   : (PRIM == kRecvReduceCopy) ? 4
                    : (int)sizeof(T);
   constexpr int KMAX = 16 / EB;
   const LL128Lane L;
@@ -293,7 +321,12 @@ __device__ __forceinline__ void ll128_slice(const RingArgs& a, const T* in, T* o
 #pragma unroll
         for (int j = 0; j < 4; j++)
           if (j >= kv) v[j] = 0.f;
-        pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+        if (PRIM == kRecvReduceCopy && sizeof(T) == 2)  // bf16 output, rounded once
+          pay = make_uint4(round_bf16_pair(v[0], v[1]), round_bf16_pair(v[2], v[3]), 0u, 0u);
+        else
+          pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+      } else if (PRIM == kCopySend) {
+        pay = kv > 0 ? load_raw_n<T>(in + e0, kv, kmax) : make_uint4(0u, 0u, 0u, 0u);  // already final
       } else {
         pay = rv[u];  // final values pass through unchanged
       }
@@ -436,6 +469,8 @@ __device__ __forceinline__ void line_slice(int prim, const RingArgs& a, const T*
       case kRecvReduceSend: ll_slice<T, kRecvReduceSend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
       case kRecvReduceCopySend: ll_slice<T, kRecvReduceCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
       case kRecvCopySend: ll_slice<T, kRecvCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
+      case kRecvReduceCopy: ll_slice<T, kRecvReduceCopy, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
+      case kCopySend: ll_slice<T, kCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
       default: ll_slice<T, kRecv, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
     }
   } else {
@@ -451,6 +486,10 @@ __device__ __forceinline__ void line_slice(int prim, const RingArgs& a, const T*
                                sslot, nelem, rf, sf, sh_abort, info, stage);
         break;
       case kRecvCopySend: ll128_slice<T, kRecvCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
+      case kRecvReduceCopy:
+        ll128_slice<T, kRecvReduceCopy, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info);
+        break;
+      case kCopySend: ll128_slice<T, kCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
       default: ll128_slice<T, kRecv, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
     }
   }
@@ -506,8 +545,10 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   while (c.valid && !sh_abort) {
     const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
     char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
-    line_slice<T, PROTO, NT>(c.prim, a, in + c.offset, out + c.offset, rslot, sslot, c.nelem, rstep, sstep,
-                             &sh_abort, info | (2u << 24) | i, stage);
+    int64_t in_off, out_off;
+    slice_offsets(a, dense, c, &in_off, &out_off);
+    line_slice<T, PROTO, NT>(c.prim, a, in + in_off, out + out_off, rslot, sslot, c.nelem, rstep, sstep, &sh_abort,
+                             info | (2u << 24) | i, stage);
     SliceCursor nx = c;
     cursor_next(g, nx);
     const uint64_t nsstep = sstep + (row_sends(c.prim) ? 1 : 0);
@@ -609,6 +650,38 @@ __device__ __forceinline__ void l8_input_piece(const char* s_in, const T* g_tile
   for (int j = 0; j < 4; j++) x[j] = j < kv ? l8_input<T>(s_in, g_tile, el + j, covered) : 0.f;
 }
 
+// The lane's kmax elements of T at tile element el as raw bits (kmax *
+// sizeof(T) = 16 or 8 bytes), zeros past kv: from shared memory when the whole
+// piece is staged, element by element otherwise.
+template <typename T>
+__device__ __forceinline__ uint4 l8_raw_piece(const char* s_in, const T* g_tile, int el, int kv, int kmax,
+                                              int covered) {
+  const int bytes = kmax * (int)sizeof(T);
+  if (kv == kmax && el + kv <= covered) {
+    if (bytes == 16) return *reinterpret_cast<const uint4*>(s_in + el * (int)sizeof(T));
+    const uint2 w = *reinterpret_cast<const uint2*>(s_in + el * (int)sizeof(T));
+    return make_uint4(w.x, w.y, 0u, 0u);
+  }
+  uint32_t wd[4] = {0u, 0u, 0u, 0u};
+  for (int j = 0; j < kv; j++) {
+    const int e = el + j;
+    uint32_t bits;
+    if (e < covered) {
+      bits = sizeof(T) == 4 ? reinterpret_cast<const uint32_t*>(s_in)[e]
+                            : (uint32_t)reinterpret_cast<const uint16_t*>(s_in)[e];
+    } else if constexpr (sizeof(T) == 4) {
+      bits = ld_cg_u32(g_tile + e);
+    } else {
+      uint16_t h;
+      asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(h) : "l"(g_tile + e) : "memory");
+      bits = h;
+    }
+    if (sizeof(T) == 4) wd[j] = bits;
+    else wd[j >> 1] |= bits << ((j & 1) * 16);
+  }
+  return make_uint4(wd[0], wd[1], wd[2], wd[3]);
+}
+
 // Check a group's flags as staged; re-poll stale lines from global memory.
 __device__ __forceinline__ bool l8_accept(const RingArgs& a, uint4& v, const char* gline, uint64_t flag, bool flag_lane,
                                           volatile int* sh_abort, uint64_t info) {
@@ -623,11 +696,11 @@ __device__ __forceinline__ void l8_tile_same_layout(const RingArgs& a, const cha
                                                     const T* g_in_tile, T* g_out_tile, const char* g_rlines,
                                                     char* g_slines, int ne, int covered, uint64_t rflag, uint64_t sflag,
                                                     volatile int* sh_abort, uint64_t info, int w) {
-  constexpr bool kIn = PRIM == kSend || PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend;
-  constexpr bool kHasRecv = PRIM != kSend;
-  constexpr bool kHasSend = PRIM != kRecv;
-  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv;
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kHasRecv = PRIM != kSend && PRIM != kCopySend;
+  constexpr bool kHasSend = PRIM != kRecv && PRIM != kRecvReduceCopy;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv ||
+                        PRIM == kRecvReduceCopy || PRIM == kCopySend;
   constexpr int EB = (PRIM == kSend || kRecvPartial) ? 4 : (int)sizeof(T);
   const LL128Lane L;
   const int kmax = L.piece_bytes / EB;
@@ -653,7 +726,12 @@ __device__ __forceinline__ void l8_tile_same_layout(const RingArgs& a, const cha
       l8_input_piece<T>(s_in, g_in_tile, el, kv, kmax, covered, x);
 #pragma unroll
       for (int j = 0; j < 4; j++) v[j] = j < kv ? (kRecvPartial ? __fadd_rn(v[j], x[j]) : x[j]) : 0.f;
-      pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+      if (PRIM == kRecvReduceCopy && sizeof(T) == 2)  // bf16 output, rounded once
+        pay = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), 0u, 0u);
+      else
+        pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+    } else if (PRIM == kCopySend) {
+      pay = l8_raw_piece<T>(s_in, g_in_tile, el, kv, kmax, covered);  // already final
     } else {
       pay = rv;  // final values pass through unchanged
     }
@@ -751,6 +829,14 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
     case kRecvCopySend:
       l8_tile_same_layout<T, kRecvCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
                                             rflag, sflag, sh_abort, info, w);
+      break;
+    case kRecvReduceCopy:
+      l8_tile_same_layout<T, kRecvReduceCopy>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne,
+                                              covered, rflag, sflag, sh_abort, info, w);
+      break;
+    case kCopySend:
+      l8_tile_same_layout<T, kCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                        rflag, sflag, sh_abort, info, w);
       break;
     default:
       l8_tile_same_layout<T, kRecv>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag,
@@ -851,7 +937,9 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
         break;
       }
       const int prim = c.prim;
-      const bool has_in = prim == kSend || prim == kRecvReduceSend || prim == kRecvReduceCopySend;
+      int64_t in_off, out_off;
+      slice_offsets(a, dense, c, &in_off, &out_off);
+      const bool has_in = row_reads_input(prim);
       const bool has_rcv = row_recvs(prim);
       const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
@@ -872,7 +960,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
         char* s_in = s_lines + kL8TileGroups * 512;
         mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
         if (b_rcv) tma_load_1d(s_lines, rslot + e0 * eb / 480 * 512, b_rcv, &bar_full[st], pol);
-        if (b_in) tma_load_1d(s_in, in + c.offset + e0, b_in, &bar_full[st], pol);
+        if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         gt++;
       }
       if (has_rcv) rstep++;
@@ -924,6 +1012,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
       const int eb_s = row_sends_partial(c.prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
+      int64_t in_off, out_off;
+      slice_offsets(a, dense, c, &in_off, &out_off);
       const int ntiles = (int)div_up(c.nelem, kL8TileElems);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
@@ -934,7 +1024,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + kL8TileGroups * 512;
         // the tile runs on every path so that the workers' barrier counts match
-        l8_tile_any<T>(c.prim, a, s_lines, s_in, in + c.offset + e0, out + c.offset + e0,
+        l8_tile_any<T>(c.prim, a, s_lines, s_in, in + in_off + e0, out + out_off + e0,
                        rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne, ne / P * P,
                        rstep + 1, sstep + 1, &sh_abort, info | (10u << 24) | i, w, &bar_fin, &fin_uses);
         __syncwarp();

@@ -174,8 +174,14 @@ def call_half(kind, n=4, count=1024, mask=0b11, proto=B.Proto.SIMPLE, flags=0, s
 def test_halves_argument_errors(lib, kind):
     S = B.Status
     assert call_half(kind, count=0) == S.OK  # empty: nothing enqueued
-    assert call_half(kind, proto=B.Proto.LL) == S.ERR_ARG  # the halves run on Simple
-    assert call_half(kind, proto=B.Proto.LL128) == S.ERR_ARG
+    # LL and LL128 need 16-byte blocks; a valid call stops at the workspace size
+    # here, before any launch (the pointers are not real)
+    for proto in (B.Proto.LL, B.Proto.LL128):
+        assert call_half(kind, proto=proto, count=1001) == S.ERR_ALIGN
+        assert call_half(kind, proto=proto, count=1002, dtype=1) == S.ERR_ALIGN
+        assert call_half(kind, proto=proto, wsb=16) == S.ERR_WORKSPACE
+        assert call_half(kind, proto=proto, count=1000, wsb=16) == S.ERR_WORKSPACE
+    assert call_half(kind, count=1001, wsb=16) == S.ERR_WORKSPACE  # Simple takes ragged blocks
     assert call_half(kind, n=1, rings=[[0]]) == S.ERR_ARG
     assert call_half(kind, rings=[[0, 1, 1, 3]]) == S.ERR_RING
     assert call_half(kind, dtype=7) == S.ERR_ARG

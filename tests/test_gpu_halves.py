@@ -13,6 +13,7 @@ from gpu_util import check_guards, device_rows_numpy, guarded_outputs, to_device
 
 pytestmark = pytest.mark.gpu
 RS, AG = oracle.REDUCE_SCATTER, oracle.ALL_GATHER
+OPROTO = {"LL": oracle.LL, "LL128": oracle.LL128, "Simple": oracle.SIMPLE}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,10 +30,11 @@ def _compare(got, want):
         assert got[r].tobytes() == want[r].tobytes(), f"rank {r}"
 
 
-def run_half(kind, n, rings, mask, count, dtype, bs=65536, cs=4, direct=False, seed=0, ws=None, in_place=False):
+def run_half(kind, n, rings, mask, count, dtype, bs=65536, cs=4, direct=False, seed=0, ws=None, in_place=False,
+             proto="Simple"):
     """One call of `kind` with blocks of `count` elements; checks it against
     the oracle and returns the workspace."""
-    ws = ws or B.Workspace(n, mask, "Simple", bs)
+    ws = ws or B.Workspace(n, mask, proto, bs)
     big_count = n * count
     if kind == RS:
         x = gen.draw("normal", n, big_count, seed, dtype)
@@ -41,7 +43,7 @@ def run_half(kind, n, rings, mask, count, dtype, bs=65536, cs=4, direct=False, s
             recv = [send[r][r * count:(r + 1) * count] for r in range(n)]
         else:
             big_out, recv = guarded_outputs(n, count, dtype)
-        B.reduce_scatter(send, recv, rings, mask, "Simple", ws, bs, cs)
+        B.reduce_scatter(send, recv, rings, mask, proto, ws, bs, cs)
     else:
         x = gen.draw("normal", n, count, seed, dtype)
         if in_place:
@@ -53,12 +55,12 @@ def run_half(kind, n, rings, mask, count, dtype, bs=65536, cs=4, direct=False, s
         else:
             big_in, send = to_device(x, dtype)
             big_out, recv = guarded_outputs(n, big_count, dtype)
-        B.all_gather(send, recv, rings, mask, "Simple", ws, bs, cs, direct=direct)
+        B.all_gather(send, recv, rings, mask, proto, ws, bs, cs, direct=direct)
     assert B.get_status(ws) == B.Status.OK
     if not (in_place and kind == RS):
         check_guards(big_out, count if kind == RS else big_count, dtype)
     got = device_rows_numpy(recv, dtype)
-    want = oracle.ring_halves_closed(kind, list(x), rings, mask, oracle.SIMPLE, bs, cs)
+    want = oracle.ring_halves_closed(kind, list(x), rings, mask, OPROTO[proto], bs, cs)
     _compare(got, want)
     return ws
 
@@ -153,3 +155,39 @@ def test_large_blocks(kind):
     n, mask, bs = 8, 0xFFF, 1 << 20
     count = 1 << 20
     run_half(kind, n, gen.ring_permutation(n, 3), mask, count, "f32", bs, 4, seed=9, direct=(kind == AG))
+
+
+# LL and LL128 take blocks of whole 16-byte pieces
+LINE_COUNTS = [8, 40, 1000, 4096, 65536, 250000, 1 << 20]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", [RS, AG])
+@pytest.mark.parametrize("proto", ["LL", "LL128"])
+@pytest.mark.parametrize("seed", range(7))
+def test_line_protocols(seed, proto, kind, dtype):
+    n, mask, bs, cs, count, rings = _random_case(300 + seed, LINE_COUNTS)
+    bs = 0 if seed % 2 else bs  # the protocol's default buffer, or a random one
+    run_half(kind, n, rings, mask, count, dtype, bs, cs, seed=seed, proto=proto)
+
+
+@pytest.mark.parametrize("proto", ["LL", "LL128"])
+def test_line_protocols_share_a_workspace(proto):
+    """The three collectives alternate on one LL / LL128 workspace (the step
+    counters, and with them the line flags, carry over from call to call)."""
+    n, mask = 5, 0x3F
+    ws = B.Workspace(n, mask, proto, 0)
+    for k in range(6):
+        dtype = "bf16" if k % 2 else "f32"
+        ring = gen.ring_permutation(n, 50 + k)
+        count = [4000, 96000, 8, 200000, 1024, 77776][k]
+        if k % 3 == 0:
+            x = gen.draw("normal", n, count, k, dtype)
+            _, send = to_device(x, dtype)
+            _, recv = guarded_outputs(n, count, dtype)
+            B.allreduce(send, recv, ring, mask, proto, ws, 0, 4)
+            assert B.get_status(ws) == B.Status.OK
+            _compare(device_rows_numpy(recv, dtype),
+                     oracle.ring_allreduce_closed(list(x), ring, mask, OPROTO[proto], 0, 4))
+        else:
+            run_half(RS if k % 3 == 1 else AG, n, ring, mask, count, dtype, 0, 4, seed=k, ws=ws, proto=proto)
