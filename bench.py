@@ -81,6 +81,23 @@ def algorithmic_bytes(case, direct=False):
     return n * 2 * s + n * 2 * (rs + ag)
 
 
+def half_algorithmic_bytes(kind, n, block, dtype, proto, direct=False):
+    """Ideal bytes of one ReduceScatter ("rs") or AllGather ("ag") call with
+    blocks of `block` elements: every rank reads its input and writes its
+    output once (n+1 blocks), plus each FIFO byte written once and read once,
+    (n-1) blocks per rank on the wire (partial sums as binary32 for
+    ReduceScatter; LL doubles, LL128 adds 1/15). Direct AllGather: no FIFO;
+    the output blocks are written once (n-1 of them by the previous rank) and
+    each rank reads back the (n-2) blocks it forwards."""
+    eb = 4 if dtype == "f32" else 2
+    m = block * eb
+    w = wire_factor(proto)
+    if kind == "ag" and direct:
+        return n * (2 * n - 1) * m
+    hop = block * 4 if kind == "rs" else m
+    return n * (n + 1) * m + 2 * n * (n - 1) * hop * w
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -184,6 +201,40 @@ def time_ring(case, torch, B, steps, warmup, direct=False):
     return ms
 
 
+def time_half(kind, n, block, ring, mask, proto, buff_size, chunk_steps, torch, B, steps, warmup, direct=False,
+              dtype="f32"):
+    """Device time per ReduceScatter / AllGather call (CUDA events)."""
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    big = torch.randn((n, n * block), generator=g, device="cuda", dtype=torch.float32).to(tdt)
+    small = torch.randn((n, block), generator=g, device="cuda", dtype=torch.float32).to(tdt)
+    ws = B.Workspace(n, mask, proto, buff_size)
+    if kind == "rs":
+        send, recv = [big[r] for r in range(n)], [small[r] for r in range(n)]
+        call = lambda: B.reduce_scatter(send, recv, ring, mask, proto, ws, buff_size, chunk_steps)  # noqa: E731
+    else:
+        send, recv = [small[r] for r in range(n)], [big[r] for r in range(n)]
+        call = lambda: B.all_gather(send, recv, ring, mask, proto, ws, buff_size, chunk_steps,  # noqa: E731
+                                    direct=direct)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    st = B.get_status(ws)
+    if st != B.Status.OK:
+        raise RuntimeError(f"{kind}: device status {st.name}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    del big, small, ws
+    return ms
+
+
 def sweep(torch, B, steps, warmup, peak):
     from collective_communication_gb300 import inputs as gen
     out = {}
@@ -199,6 +250,23 @@ def sweep(torch, B, steps, warmup, peak):
             "us": round(t * 1e6, 1),
             "roofline_frac": round(algorithmic_bytes(c, direct) / t / 1e9 / peak, 3),
             "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
+    # the halves: N=8, 12 channels, the headline's ring, 8 MiB f32 blocks (the
+    # 64 MiB per-rank buffer of the AllReduce); busBW = n*block bytes / t *
+    # (N-1)/N, the usual convention for these collectives
+    hc = cases[0]
+    block = 64 * gen.MIB // 4 // 8
+    for kind, proto, bs, direct in (("rs", "Simple", gen.MIB, False), ("ag", "Simple", gen.MIB, False),
+                                    ("ag", "Simple", gen.MIB, True), ("rs", "LL128", 0, False),
+                                    ("ag", "LL128", 0, False)):
+        ms = time_half(kind, 8, block, hc.ring, 0xFFF, proto, bs, 4, torch, B, steps, warmup, direct)
+        t = statistics.median(ms) / 1e3
+        name = {"rs": "reduce_scatter", "ag": "all_gather"}[kind]
+        tag = f"{proto.lower()}{bs // gen.KIB}k" if bs else proto.lower()
+        total = 8 * block * 4
+        out[f"n8_{name}_{tag}_ch12_64MiB" + ("_direct" if direct else "")] = {
+            "busbw_gbs": round(total / t * 7 / 8 / 1e9, 2),
+            "us": round(t * 1e6, 1),
+            "roofline_frac": round(half_algorithmic_bytes(kind, 8, block, "f32", proto, direct) / t / 1e9 / peak, 3)}
     # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel. Device
     # latency from a CUDA graph of back-to-back calls (no host enqueue time),
     # and the stream-launch latency as seen between two events.

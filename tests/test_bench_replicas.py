@@ -50,3 +50,22 @@ def test_replicas_take_the_slowest_time_and_sum_the_bytes():
     assert single_ms == pytest.approx(5.0)
     # busBW of one replica: S / t * 2(N-1)/N
     assert single_value == pytest.approx((64 << 20) / 5e-3 * 2 * 7 / 8 / 1e9)
+
+
+def test_algorithmic_bytes_of_the_halves_add_up_to_the_allreduce():
+    """ReduceScatter then AllGather move the AllReduce's bytes plus the
+    intermediate block, written once and read once (2 blocks per rank)."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from collective_communication_gb300 import inputs as gen
+    for n, dtype, proto in ((8, "f32", "Simple"), (4, "bf16", "LL128"), (3, "f32", "LL")):
+        block = 3000
+        eb = 4 if dtype == "f32" else 2
+        case = gen.RingCase("x", n, list(range(n)), 1, proto, n * block, dtype, "normal", 0, 0, 4)
+        ar = bench.algorithmic_bytes(case)
+        halves = (bench.half_algorithmic_bytes("rs", n, block, dtype, proto) +
+                  bench.half_algorithmic_bytes("ag", n, block, dtype, proto))
+        assert halves == pytest.approx(ar + 2 * n * block * eb)
+    # direct AllGather: outputs written once, (n-2) blocks read back, one input block read
+    assert bench.half_algorithmic_bytes("ag", 8, 10, "f32", "Simple", True) == 8 * (8 + 1 + 6) * 40
