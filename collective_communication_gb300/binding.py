@@ -42,6 +42,7 @@ EXPORTED = (
     "rar_workspace_bytes", "rar_workspace_init", "rar_allreduce", "rar_oneshot", "rar_get_status",
     "rar_strerror", "rar_set_spin_timeout_ns", "rar_debug_set_fault", "rar_describe_geometry",
     "rar_allreduce_static", "rar_allreduce_ex", "rar_reduce_scatter", "rar_all_gather",
+    "rar_oneshot_workspace_bytes", "rar_oneshot_workspace_init", "rar_oneshot_staged",
 )
 
 
@@ -92,6 +93,12 @@ def load_library():
     L.rar_reduce_scatter.restype = I
     L.rar_all_gather.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I, ctypes.c_uint, P, SZ, P]
     L.rar_all_gather.restype = I
+    L.rar_oneshot_workspace_bytes.argtypes = [I, SZ, I]
+    L.rar_oneshot_workspace_bytes.restype = SZ
+    L.rar_oneshot_workspace_init.argtypes = [P, SZ, I, SZ, I, P]
+    L.rar_oneshot_workspace_init.restype = I
+    L.rar_oneshot_staged.argtypes = [P, P, I, SZ, I, I, P, SZ, P]
+    L.rar_oneshot_staged.restype = I
     _lib = L
     return L
 
@@ -238,7 +245,50 @@ def oneshot(sendbufs: Sequence, recvbufs: Sequence, stream=None) -> None:
     _check(st, "rar_oneshot")
 
 
-def get_status(workspace: Workspace, stream=None) -> Status:
+class OneShotWorkspace:
+    """Device workspace of the staged one-shot (torch-allocated, 256-byte
+    aligned), initialised for calls of up to max_count elements."""
+
+    def __init__(self, nranks: int, max_count: int, dtype, device=None, stream=None):
+        import torch
+        if dtype in ("f32", "bf16"):
+            dt = Dtype.F32 if dtype == "f32" else Dtype.BF16
+        elif isinstance(dtype, torch.dtype):
+            dt = Dtype.F32 if dtype == torch.float32 else Dtype.BF16 if dtype == torch.bfloat16 else None
+        else:
+            dt = Dtype(dtype)
+        if dt is None:
+            raise TypeError(f"unsupported dtype {dtype} (float32 or bfloat16)")
+        self.nbytes = int(load_library().rar_oneshot_workspace_bytes(nranks, max_count, int(dt)))
+        if self.nbytes == 0:
+            raise RarError(Status.ERR_ARG, "rar_oneshot_workspace_bytes")
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device or "cuda")
+        base = self.buf.data_ptr()
+        self._ptr = (base + 255) // 256 * 256
+        self.nranks, self.max_count, self.dtype = nranks, max_count, dt
+        self.init(stream)
+
+    def init(self, stream=None):
+        """(Re-)initialise: zero the counters, record the configuration."""
+        _check(load_library().rar_oneshot_workspace_init(self._ptr, self.nbytes, self.nranks, self.max_count,
+                                                          int(self.dtype), _stream_handle(stream)),
+               "rar_oneshot_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self._ptr
+
+
+def oneshot_staged(sendbufs: Sequence, recvbufs: Sequence, workspace: OneShotWorkspace, stream=None) -> None:
+    """Enqueue one staged one-shot AllReduce (sum) over len(sendbufs) ranks."""
+    n = len(sendbufs)
+    st = load_library().rar_oneshot_staged(_ptrs(sendbufs), _ptrs(recvbufs), n, sendbufs[0].numel(),
+                                           int(_dtype_of(sendbufs[0])), 0, workspace.ptr, workspace.nbytes,
+                                           _stream_handle(stream))
+    _check(st, "rar_oneshot_staged")
+
+
+def get_status(workspace, stream=None) -> Status:
     return Status(load_library().rar_get_status(workspace.ptr, _stream_handle(stream)))
 
 

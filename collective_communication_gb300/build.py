@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librar.so")
-SOURCES = ["rar_api.cu", "ring_simple.cu", "ring_ll.cu", "oneshot.cu", "rar_static_ws.cu"]
+SOURCES = ["rar_api.cu", "ring_simple.cu", "ring_ll.cu", "oneshot.cu", "oneshot_staged.cu", "rar_static_ws.cu"]
 HEADERS = ["rar_device.cuh", "rar_geometry.h", "rar_launch.h"]
 
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -100,6 +100,37 @@ rar_status from_cuda(cudaError_t e) {
   return RAR_ERR_CUDA;
 }
 
+__global__ void init_staged_header_kernel(char* ws, int nranks, int dtype, int blocks_per_rank, int64_t max_count,
+                                          int64_t slot_bytes) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    OsHeader* h = reinterpret_cast<OsHeader*>(ws);
+    h->status = 0;
+    h->abort = 0;
+    h->nranks = nranks;
+    h->dtype = dtype;
+    h->blocks_per_rank = blocks_per_rank;
+    h->max_count = max_count;
+    h->slot_bytes = slot_bytes;
+    h->err_info = 0;
+    h->err_step = 0;
+    h->magic = kStagedMagic;
+  }
+}
+
+cudaError_t device_sms(int* sms) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  static int cache[64] = {0};
+  if (device < 64 && cache[device] != 0) {
+    *sms = cache[device];
+    return cudaSuccess;
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device);
+  if (e == cudaSuccess && device < 64) cache[device] = *sms;
+  return e;
+}
+
 __global__ void init_header_kernel(char* ws, int nranks, uint64_t mask, int proto, int64_t buff_size) {
   if (threadIdx.x == 0 && blockIdx.x == 0) {
     WsHeader* h = reinterpret_cast<WsHeader*>(ws);
@@ -283,6 +314,69 @@ rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbufs, int n
   a.dtype = (int)dtype;
   a.count = (int64_t)count;
   return from_cuda(launch_oneshot(a, (cudaStream_t)stream));
+}
+
+size_t rar_oneshot_workspace_bytes(int nranks, size_t max_count, rar_dtype dtype) {
+  if (nranks < 1 || nranks > kMaxRanks) return 0;
+  if (dtype != RAR_F32 && dtype != RAR_BF16) return 0;
+  if (max_count == 0 || max_count > (size_t)INT64_MAX / 64 / (size_t)nranks) return 0;
+  return (size_t)staged_workspace_bytes(nranks, (int64_t)max_count, dtype == RAR_F32 ? 4 : 2);
+}
+
+rar_status rar_oneshot_workspace_init(void* workspace, size_t workspaceBytes, int nranks, size_t max_count,
+                                      rar_dtype dtype, void* stream) {
+  const size_t need = rar_oneshot_workspace_bytes(nranks, max_count, dtype);
+  if (need == 0) return RAR_ERR_ARG;
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
+  if (workspaceBytes < need) return RAR_ERR_WORKSPACE;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return from_cuda(e);
+  cudaStream_t s = (cudaStream_t)stream;
+  // header and counters only: a slot's bytes are always written before they are read
+  e = cudaMemsetAsync(workspace, 0, (size_t)staged_stage_offset(nranks), s);
+  if (e != cudaSuccess) return from_cuda(e);
+  const int eb = dtype == RAR_F32 ? 4 : 2;
+  init_staged_header_kernel<<<1, 32, 0, s>>>((char*)workspace, nranks, (int)dtype,
+                                             staged_blocks_per_rank(nranks, sms), (int64_t)max_count,
+                                             staged_slot_bytes((int64_t)max_count, eb));
+  return from_cuda(cudaGetLastError());
+}
+
+rar_status rar_oneshot_staged(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                              rar_dtype dtype, rar_redop op, void* workspace, size_t workspaceBytes, void* stream) {
+  if (op != RAR_SUM) return RAR_ERR_ARG;
+  if (nranks < 1 || nranks > kMaxRanks) return RAR_ERR_ARG;
+  if (dtype != RAR_F32 && dtype != RAR_BF16) return RAR_ERR_ARG;
+  if (count > (size_t)INT64_MAX / 64 / (size_t)nranks) return RAR_ERR_ARG;
+  const int eb = dtype == RAR_F32 ? 4 : 2;
+  rar_status st = check_buffers(sendbufs, recvbufs, nranks, (int64_t)count * eb, true);
+  if (st != RAR_OK) return st;
+  if (workspace == nullptr) return RAR_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
+  // An empty call enqueues nothing and advances no sequence number ([OS89],
+  // review of the empty-input case).
+  if (count == 0) return RAR_OK;
+  if ((int64_t)workspaceBytes < staged_workspace_bytes(nranks, (int64_t)count, eb)) return RAR_ERR_WORKSPACE;
+  int sms = 0;
+  cudaError_t e = device_sms(&sms);
+  if (e != cudaSuccess) return from_cuda(e);
+  StagedArgs a;
+  std::memset(&a, 0, sizeof a);
+  for (int r = 0; r < nranks; r++) {
+    a.send[r] = sendbufs[r];
+    a.recv[r] = recvbufs[r];
+  }
+  a.nranks = nranks;
+  a.dtype = (int)dtype;
+  a.blocks_per_rank = staged_blocks_per_rank(nranks, sms);
+  a.fault = g_fault.load(std::memory_order_relaxed);
+  a.count = (int64_t)count;
+  a.ws = (char*)workspace;
+  a.stage_offset = staged_stage_offset(nranks);  // the slot size comes from the workspace header
+  a.timeout_ns = spin_timeout_ns();
+  return from_cuda(launch_oneshot_staged(a, (cudaStream_t)stream));
 }
 
 rar_status rar_get_status(void* workspace, void* stream) {

@@ -68,6 +68,7 @@ constexpr uint32_t kErrAbort = 8;
 // of time and the launch ends with RAR_ERR_TIMEOUT).
 constexpr int kFaultNone = 0;
 constexpr int kFaultDropHead = 1;   // receivers never publish their head
+constexpr int kFaultDropAck = 2;    // staged one-shot: ranks never acknowledge their reads
 
 struct RingArgs {
   const void* send[kMaxRanks];
@@ -113,6 +114,15 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Returns the old value.
+__device__ __forceinline__ uint64_t atom_add_acq_rel_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
 
 // FIFO payload reads: cached in L2 only, so a slot reused NCCL_STEPS steps
 // later is never served from a stale L1 line.
@@ -232,7 +242,10 @@ __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ WsHeader* header_of(const RingArgs& a) { return (WsHeader*)a.ws; }
 
-__device__ __forceinline__ void report_failure(WsHeader* h, uint32_t code, uint64_t info, uint64_t step) {
+// First failure wins the status word; every failure raises the abort flag.
+// H: any workspace header with status, abort, err_info and err_step.
+template <typename H>
+__device__ __forceinline__ void report_failure(H* h, uint32_t code, uint64_t info, uint64_t step) {
   if (atomicCAS(&h->status, 0u, code) == 0u) {
     h->err_info = info;
     h->err_step = step;
@@ -251,17 +264,20 @@ struct Spin {
   uint32_t iters;
   uint32_t checks;
   __device__ __forceinline__ Spin() : t0(0), iters(0), checks(0) {}
-  __device__ __forceinline__ bool poll(const RingArgs& a, uint64_t info, uint64_t step) {
+  template <typename H>
+  __device__ __forceinline__ bool poll_h(H* h, uint64_t timeout_ns, uint64_t info, uint64_t step) {
     if ((++iters & 63u) != 0u) return false;
-    WsHeader* h = header_of(a);
     if (ld_relaxed_u32(&h->abort) != 0u) return true;
     uint64_t now = global_timer_ns();
     if (t0 == 0) t0 = now;
-    if (now - t0 > a.timeout_ns || ++checks > kMaxSpinChecks) {
+    if (now - t0 > timeout_ns || ++checks > kMaxSpinChecks) {
       report_failure(h, kErrTimeout, info, step);
       return true;
     }
     return false;
+  }
+  __device__ __forceinline__ bool poll(const RingArgs& a, uint64_t info, uint64_t step) {
+    return poll_h(header_of(a), a.timeout_ns, info, step);
   }
 };
 

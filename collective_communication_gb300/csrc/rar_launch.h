@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #include "rar_device.cuh"
 
@@ -19,5 +20,62 @@ struct OneShotArgs {
   int64_t count;
 };
 cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream);
+
+// ---- staged one-shot (oneshot_staged.cu) ----
+// Workspace: a 4 KiB header, one OsControl per rank (rounded up to 4 KiB),
+// then kStagingSlots slots of slot_bytes per rank.
+constexpr uint32_t kStagedMagic = 0x31534152u;  // "RAS1"
+constexpr int kStagingSlots = 4;                // slots per rank, reused round-robin
+constexpr int kStagedBlocksPerSm = 2;           // grid = nranks * (SMs * 2 / nranks) blocks
+
+struct OsHeader {
+  uint32_t magic;
+  uint32_t status;  // first device failure (rar_status), 0 if none: same offset as the ring header's
+  uint32_t abort;
+  int32_t nranks;
+  int32_t dtype;
+  int32_t blocks_per_rank;
+  int64_t max_count;   // elements a slot holds
+  int64_t slot_bytes;
+  uint64_t err_info;
+  uint64_t err_step;
+};
+static_assert(offsetof(OsHeader, status) == offsetof(WsHeader, status), "status word at one offset");
+
+// Per-rank sequence numbers and counters, each on its own 128-byte line; all
+// monotonic across calls.
+struct OsControl {
+  uint64_t tx_seq;  // calls whose slot this rank has completely written
+  uint64_t pad0[15];
+  uint64_t ack_seq;  // calls whose slots this rank has completely read
+  uint64_t pad1[15];
+  uint64_t done;  // blocks that finished copying, over all calls
+  uint64_t pad2[15];
+  uint64_t read;  // blocks that finished reducing, over all calls
+  uint64_t pad3[15];
+};
+
+struct StagedArgs {
+  const void* send[kMaxRanks];
+  void* recv[kMaxRanks];
+  int nranks;
+  int dtype;
+  int blocks_per_rank;
+  int fault;
+  int64_t count;
+  char* ws;
+  int64_t stage_offset;
+  uint64_t timeout_ns;
+};
+
+inline int64_t staged_slot_bytes(int64_t max_count, int elem_bytes) { return align_up(max_count * elem_bytes, 256); }
+inline int64_t staged_stage_offset(int nranks) {
+  return kHeaderBytes + align_up((int64_t)nranks * (int64_t)sizeof(OsControl), 4096);
+}
+inline int64_t staged_workspace_bytes(int nranks, int64_t max_count, int elem_bytes) {
+  return staged_stage_offset(nranks) + (int64_t)nranks * kStagingSlots * staged_slot_bytes(max_count, elem_bytes);
+}
+int staged_blocks_per_rank(int nranks, int sms);
+cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream);
 
 }  // namespace rar

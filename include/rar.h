@@ -231,6 +231,44 @@ RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbuf
                        size_t count, rar_dtype dtype, rar_redop op, void* stream);
 
 /*
+ * Staged one-shot AllReduce (sum), the single-kernel form of [OS89] (the
+ * "5 kernels -> 3" review and its one-kernel follow-up): per call every rank
+ * copies its input into a staging slot of the workspace, the last of the
+ * rank's blocks to finish copying (found with a monotonic done counter that
+ * every launch advances by exactly its fixed grid) publishes the rank's
+ * sequence number, every block waits for all ranks' numbers, then each rank
+ * reduces the nranks staged copies:
+ *   recvbufs[r][i] = T(((x_0[i] + x_1[i]) + x_2[i]) + ... + x_{n-1}[i])
+ * in binary32, in user-rank order, rounded once for bf16 (the same value as
+ * rar_oneshot). A slot is reused every 4 calls and only after every rank has
+ * acknowledged reading it (the guard). Nothing is reset between calls, so a
+ * CUDA graph of calls may be replayed any number of times.
+ *
+ * rar_oneshot_workspace_bytes: bytes of a workspace for calls of up to
+ *   max_count elements of dtype over nranks ranks (0 for invalid arguments):
+ *   a 4 KiB header, 512 B of counters per rank, 4 slots per rank.
+ * rar_oneshot_workspace_init: zero the header and counters, record the
+ *   configuration (nranks, dtype, max_count, and the grid, 2 * SMs / nranks
+ *   blocks per rank on the current device); enqueued on `stream`. Errors:
+ *   RAR_ERR_ARG, RAR_ERR_WORKSPACE (null or too small), RAR_ERR_ALIGN (not
+ *   256-byte aligned), RAR_ERR_CUDA.
+ * rar_oneshot_staged: sendbufs/recvbufs as for rar_oneshot, except that in
+ *   place (recvbufs[r] == sendbufs[r]) is allowed: every rank reads only the
+ *   staged copies. count 0 returns RAR_OK and advances nothing. The workspace
+ *   must have been initialised for (nranks, dtype) with max_count >= count on
+ *   this device, else the kernel reports RAR_ERR_WORKSPACE through
+ *   rar_get_status(); a wait that runs out of time (rar_set_spin_timeout_ns)
+ *   reports RAR_ERR_TIMEOUT and leaves the workspace aborted (re-initialise).
+ *   The launch is cooperative: RAR_ERR_CORESIDENCY if it cannot be resident.
+ */
+RAR_API size_t rar_oneshot_workspace_bytes(int nranks, size_t max_count, rar_dtype dtype);
+RAR_API rar_status rar_oneshot_workspace_init(void* workspace, size_t workspaceBytes, int nranks,
+                                              size_t max_count, rar_dtype dtype, void* stream);
+RAR_API rar_status rar_oneshot_staged(const void* const* sendbufs, void* const* recvbufs, int nranks,
+                                      size_t count, rar_dtype dtype, rar_redop op, void* workspace,
+                                      size_t workspaceBytes, void* stream);
+
+/*
  * Bytes of the device array behind rar_allreduce_static(). Every GPU that
  * loads this library holds one such array until the process exits.
  */
@@ -292,7 +330,9 @@ RAR_API void rar_set_spin_timeout_ns(uint64_t ns);
 /*
  * Test hook for failure detection: fault 0 = none (default); 1 = every
  * receiver skips publishing its head, so each sender runs out of credit
- * after RAR_NCCL_STEPS steps and waits until the time limit. No GPU fault
+ * after RAR_NCCL_STEPS steps and waits until the time limit; 2 = in
+ * rar_oneshot_staged, no rank acknowledges its reads, so the fifth call's
+ * guard (4 slots per rank) waits until the time limit. No GPU fault
  * happens: the waits end, every block leaves, the launch completes, and
  * rar_get_status() reports RAR_ERR_TIMEOUT. Applies to launches enqueued
  * after the call.

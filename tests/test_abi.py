@@ -220,3 +220,47 @@ def test_halves_buffer_overlap_rules(lib, kind):
         assert call_half(kind, send=[base[1]] + other[1:], recv=base) == S.ERR_ARG
     # two receive buffers overlapping
     assert call_half(kind, send=other, recv=[base[0], base[0] + 16] + base[2:]) == S.ERR_ARG
+
+
+def test_staged_oneshot_workspace_bytes_formula(lib):
+    L = B.load_library()
+    for n in (1, 2, 8, 32):
+        for count, dt, eb in ((1, 0, 4), (7168 * 512, 1, 2), (1000, 1, 2), (4097, 0, 4)):
+            slot = -(-count * eb // 256) * 256
+            want = 4096 + -(-n * 512 // 4096) * 4096 + n * 4 * slot
+            assert L.rar_oneshot_workspace_bytes(n, count, dt) == want
+    assert L.rar_oneshot_workspace_bytes(0, 10, 0) == 0
+    assert L.rar_oneshot_workspace_bytes(33, 10, 0) == 0
+    assert L.rar_oneshot_workspace_bytes(4, 0, 0) == 0
+    assert L.rar_oneshot_workspace_bytes(4, 10, 5) == 0
+
+
+def call_staged(n=4, count=1024, dtype=0, op=0, send=None, recv=None, ws=FAKE, wsb=1 << 30):
+    send = [FAKE + (i << 28) for i in range(n)] if send is None else send
+    recv = [FAKE + (1 << 35) + (i << 28) for i in range(n)] if recv is None else recv
+    L = B.load_library()
+    sp = (ctypes.c_void_p * n)(*send)
+    rp = (ctypes.c_void_p * n)(*recv)
+    return L.rar_oneshot_staged(sp, rp, n, count, dtype, op, ws, wsb, None)
+
+
+def test_staged_oneshot_argument_errors(lib):
+    S = B.Status
+    L = B.load_library()
+    assert call_staged(count=0) == S.OK  # empty: nothing enqueued, nothing advanced
+    assert call_staged(op=1) == S.ERR_ARG
+    assert call_staged(dtype=3) == S.ERR_ARG
+    assert call_staged(n=0, send=[], recv=[]) == S.ERR_ARG
+    assert call_staged(send=[FAKE + 8] + [FAKE + (i << 28) for i in range(1, 4)]) == S.ERR_ALIGN
+    assert call_staged(ws=0) == S.ERR_WORKSPACE
+    assert call_staged(ws=FAKE + 16) == S.ERR_ALIGN
+    assert call_staged(wsb=4096) == S.ERR_WORKSPACE  # too small for this count
+    # in place is allowed (only staged copies are read); other overlaps are not
+    base = [FAKE + (i << 28) for i in range(4)]
+    assert call_staged(send=base, recv=base, wsb=4096) == S.ERR_WORKSPACE  # passed the buffer checks
+    assert call_staged(send=base, recv=[base[1]] + base[1:]) == S.ERR_ARG
+    # init: argument errors before any device work
+    assert L.rar_oneshot_workspace_init(None, 1 << 30, 4, 1024, 0, None) == S.ERR_WORKSPACE
+    assert L.rar_oneshot_workspace_init(FAKE + 16, 1 << 30, 4, 1024, 0, None) == S.ERR_ALIGN
+    assert L.rar_oneshot_workspace_init(FAKE, 4096, 4, 1024, 0, None) == S.ERR_WORKSPACE
+    assert L.rar_oneshot_workspace_init(FAKE, 1 << 30, 0, 1024, 0, None) == S.ERR_ARG
