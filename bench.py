@@ -321,6 +321,25 @@ def sweep(torch, B, steps, warmup, peak):
         tg = gl * 1e-6 if gl else t
         out[case.name] = {"stream_us": round(t * 1e6, 2), "graph_us": gl,
                           "unique_bytes_frac": round(2 * case.nranks * nbytes / tg / 1e9 / peak, 3)}
+        # the staged form (copy into slots, sequence numbers, reduce): unique
+        # bytes 4 * N * S (the copy's read and write added to the direct form's)
+        ws = B.OneShotWorkspace(case.nranks, case.count, "bf16")
+        for _ in range(warmup):
+            B.oneshot_staged(send, recv, ws)
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record(s)
+            B.oneshot_staged(send, recv, ws)
+            b.record(s)
+        torch.cuda.synchronize()
+        if B.get_status(ws) != B.Status.OK:
+            raise RuntimeError("staged one-shot: device status")
+        t = statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
+        gl = graph_latency(lambda: B.oneshot_staged(send, recv, ws), torch)
+        tg = gl * 1e-6 if gl else t
+        out[case.name + "_staged"] = {"stream_us": round(t * 1e6, 2), "graph_us": gl,
+                                      "unique_bytes_frac": round(4 * case.nranks * nbytes / tg / 1e9 / peak, 3)}
+        del ws
     return out
 
 
