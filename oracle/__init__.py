@@ -73,6 +73,7 @@ def lib():
         L.orc_ring_allreduce_closed.argtypes = [P, P, I, SZ, I, P, I, U64, I, SZ, I]
         L.orc_ring_collective_sim.argtypes = [I, P, P, I, SZ, I, P, I, U64, I, SZ, I, I, P, P, P]
         L.orc_ring_halves_closed.argtypes = [I, P, P, I, SZ, I, P, I, U64, I, SZ, I]
+        L.orc_ll_session_sim.argtypes = [I, P, P, P, I, I, P, I, U64, SZ, ctypes.c_uint32, I, P, P]
         L.orc_ring_closed_at.argtypes = [P, I, SZ, I, P, I, U64, I, SZ, I, P, SZ, P, P]
         L.orc_oneshot.argtypes = [P, P, I, SZ, I]
         L.orc_state_model.argtypes = [I, I, I, I, P]
@@ -320,6 +321,35 @@ def ring_halves_closed(kind, inputs, ring_order, mask, proto, buff_size=0, chunk
                                       nrings, mask, proto, buff_size, chunk_steps)
     _check(st, "ring_halves_closed")
     return outs
+
+
+def ll_session_sim(calls, ring_order, mask, buff_size=0, flag_max=0, cleanup=True):
+    """A sequence of LL ring AllReduce calls on one workspace (FIFOs and step
+    counters persist). calls: list of per-rank input lists (one list per call,
+    each of nranks equal-length arrays). flag_max 0: production flags, else the
+    wrap period (a power of two >= 64). Returns (outputs per call,
+    stale_accepts, max_stale_age)."""
+    n = len(calls[0])
+    ins, outs, counts = [], [], []
+    for c in calls:
+        arrs, dt = _prep(c)
+        if len(arrs) != n:
+            raise ValueError("every call needs nranks inputs")
+        ins.extend(arrs)
+        outs.extend(np.zeros_like(a) for a in arrs)
+        counts.append(arrs[0].size)
+    dts = {_dtype_code(a) for a in ins}
+    if len(dts) != 1:
+        raise ValueError("one dtype for the whole session")
+    rings, nrings = _rings(ring_order)
+    cnt = np.ascontiguousarray(np.asarray(counts, np.uint64))
+    stale = np.zeros(1, np.int64)
+    age = np.zeros(1, np.int64)
+    st = lib().orc_ll_session_sim(len(calls), _ptr(cnt), _ptr_array(ins), _ptr_array(outs), n, dts.pop(),
+                                  _ptr(rings), nrings, mask, buff_size, flag_max, int(cleanup), _ptr(stale),
+                                  _ptr(age))
+    _check(st, "ll_session_sim")
+    return [outs[k * n:(k + 1) * n] for k in range(len(calls))], int(stale[0]), int(age[0])
 
 
 def oneshot(inputs):

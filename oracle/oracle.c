@@ -508,7 +508,15 @@ size_t orc_ll128_decode(const uint64_t* lines, size_t nbytes, uint64_t flag, uin
 typedef struct {
   uint8_t* fifo;
   uint64_t head, tail;
+  /* LL sessions only (orc_ll_session_sim): per line of the FIFO, the step its
+   * content was written for (NEVER if never written); the receiver's lines of
+   * the pending slice accepted so far, and their payload */
+  uint64_t* wstep;
+  uint8_t* acc;
+  uint8_t* pbuf;
 } conn_t;
+
+#define NEVER UINT64_MAX
 
 typedef struct {
   const geom_t* g;
@@ -523,7 +531,30 @@ typedef struct {
   uint8_t* pay_out;
   float* vals;              /* scratch binary32 values */
   int direct;               /* Simple only: all-gather hops write the next rank's output */
+  /* LL sessions: line-by-line acceptance, the flag period and its cleanup */
+  int session;
+  uint32_t flag_max;        /* 0: flag = step + 1 (32 bits); else (step + 1) mod flag_max */
+  int cleanup;
+  int64_t stale_accepts;    /* lines accepted whose content was written for another step */
+  int64_t max_stale_age;    /* largest step distance of a stale line a receiver polled */
 } sim_t;
+
+/* LL flag of a step ([C23] "LL：Data 与 Flag 同 Line": production flag = step + 1;
+ * the test mode wraps it at 0x100). */
+static uint32_t ll_flag_of(const sim_t* S, uint64_t step) {
+  return S->flag_max ? (uint32_t)((step + 1) % S->flag_max) : (uint32_t)(step + 1);
+}
+
+/* Reading of the page's cleanup: the sender rewrites the rest of its slot
+ * (every line past its slice) with the current flag on the last NCCL_STEPS
+ * steps of every half flag period, i.e. once per slot every flag_max/2 steps.
+ * A line of a slot is then never older than flag_max/2 steps when it is read,
+ * so no stale line can carry the flag of the step being read. */
+static int ll_cleanup_step(const sim_t* S, uint64_t step) {
+  if (!S->cleanup || S->flag_max == 0) return 0;
+  uint64_t half = S->flag_max / 2;
+  return step % half >= half - NSTEPS;
+}
 
 /* One slice of one rank's program. */
 typedef struct {
@@ -578,6 +609,31 @@ static int fifo_try_recv(sim_t* S, int e, uint64_t step, size_t nbytes) {
   const geom_t* g = S->g;
   conn_t* c = &S->conn[e];
   uint8_t* slot = c->fifo + (step % NSTEPS) * g->step_bytes;
+  if (S->session) {
+    /* every line on its own, as the GPU's threads poll theirs: a line whose
+     * two flags equal the step's flag is taken, whenever it was written */
+    uint32_t flag = ll_flag_of(S, step);
+    size_t nlines = div_up(nbytes, 8), line0 = (step % NSTEPS) * (g->step_bytes / 16);
+    const uint32_t* L = (const uint32_t*)slot;
+    int all = 1;
+    for (size_t j = 0; j < nlines; j++) {
+      if (c->acc[j]) continue;
+      uint64_t ws = c->wstep[line0 + j];
+      if (ws != step && ws != NEVER && (int64_t)(step - ws) > S->max_stale_age) S->max_stale_age = (int64_t)(step - ws);
+      if (L[4 * j + 1] == flag && L[4 * j + 3] == flag) {
+        memcpy(c->pbuf + 8 * j, &L[4 * j], 4);
+        memcpy(c->pbuf + 8 * j + 4, &L[4 * j + 2], 4);
+        c->acc[j] = 1;
+        if (ws != step) S->stale_accepts++;
+      } else {
+        all = 0;
+      }
+    }
+    if (!all) return 0;
+    memcpy(S->pay_in, c->pbuf, nbytes);
+    memset(c->acc, 0, nlines);
+    return 1;
+  }
   if (g->proto == ORC_SIMPLE) {
     if (c->tail < step + (uint64_t)g->sps) return 0;
     memcpy(S->pay_in, slot, nbytes);
@@ -603,6 +659,22 @@ static int fifo_send(sim_t* S, int e, uint64_t step, size_t nbytes) {
     if (nbytes > (size_t)g->sps * g->step_bytes) return ORC_ECHECK;
     memcpy(slot, S->pay_out, nbytes);
     c->tail = step + (uint64_t)g->sps; /* payload first, then the tail */
+  } else if (g->proto == ORC_LL && S->session) {
+    size_t nlines = div_up(nbytes, 8), slines = g->step_bytes / 16, line0 = (step % NSTEPS) * slines;
+    if (nlines > slines) return ORC_ECHECK;
+    uint32_t flag = ll_flag_of(S, step);
+    orc_ll_encode(S->pay_out, nbytes, flag, (uint32_t*)slot);
+    for (size_t j = 0; j < nlines; j++) c->wstep[line0 + j] = step;
+    if (ll_cleanup_step(S, step)) {
+      uint32_t* L = (uint32_t*)slot;
+      for (size_t j = nlines; j < slines; j++) {
+        L[4 * j] = 0;
+        L[4 * j + 1] = flag;
+        L[4 * j + 2] = 0;
+        L[4 * j + 3] = flag;
+        c->wstep[line0 + j] = step;
+      }
+    }
   } else if (g->proto == ORC_LL) {
     if (div_up(nbytes, 8) * 16 > g->step_bytes) return ORC_ECHECK;
     orc_ll_encode(S->pay_out, nbytes, (uint32_t)(step + 1), (uint32_t*)slot);
@@ -860,6 +932,131 @@ int orc_ring_allreduce_sim(const void* const* send, void* const* recv, int nrank
                            int64_t* loops_out) {
   return orc_ring_collective_sim(ORC_ALLREDUCE, send, recv, nranks, count, dtype, ring_order, nrings, mask,
                                  proto, buffSize, chunkSteps, direct, sends, recvs, loops_out);
+}
+
+/*
+ * A sequence of ring AllReduce calls on one LL workspace, as the library runs
+ * them: the connector FIFOs and every rank's step counters persist from call
+ * to call (nothing is cleared between calls, [C23] "LL：Data 与 Flag 同 Line":
+ * the monotonic generation makes old lines mismatch). Receivers take each
+ * 16-byte line on its own as soon as both its flags equal the step's flag,
+ * the way the GPU's threads poll their lines, so a stale line that happens to
+ * carry the right flag is taken: the simulation counts such lines.
+ *
+ * Call k uses counts[k] elements per rank, send[k*nranks + r] and
+ * recv[k*nranks + r]. flag_max 0: production flags (step + 1, 32 bits);
+ * otherwise a power of two >= 64, flags (step + 1) mod flag_max (the page's
+ * test mode wraps at 0x100), with the slot cleanup when `cleanup` is set
+ * (tests turn it off to show what it prevents). Outputs: stale_accepts (lines
+ * taken whose content was written for another step) and max_stale_age (the
+ * largest step distance between a polled stale line's write and the poll).
+ */
+int orc_ll_session_sim(int ncalls, const size_t* counts, const void* const* send, void* const* recv,
+                       int nranks, int dtype, const int* ring_order, int nrings, uint64_t mask,
+                       size_t buffSize, uint32_t flag_max, int cleanup, int64_t* stale_accepts,
+                       int64_t* max_stale_age) {
+  if (ncalls < 0) return ORC_EARG;
+  if (flag_max != 0 && (flag_max < 64 || (flag_max & (flag_max - 1)) != 0)) return ORC_EARG;
+  geom_t g;
+  int st = geom_init(&g, ORC_LL, dtype, nranks, mask, 0, buffSize, 4);
+  if (st != ORC_OK) return st;
+  if (nrings != 1 && nrings != g.nchan) return ORC_EARG;
+  int rank_at[MAXR];
+  for (int ch = 0; ch < nrings; ch++) {
+    st = rank_at_index(nranks, ring_order + (size_t)ch * nranks, rank_at);
+    if (st != ORC_OK) return st;
+  }
+  size_t nconn = (size_t)g.nchan * nranks, slines = g.step_bytes / 16;
+  conn_t* conn = calloc(nconn, sizeof(conn_t));
+  uint8_t* fifo = calloc(nconn * NSTEPS, g.step_bytes);
+  uint64_t* wstep = malloc(sizeof(uint64_t) * nconn * NSTEPS * slines);
+  uint8_t* acc = calloc(nconn, slines);
+  uint8_t* pbuf = calloc(nconn, slines * 8);
+  uint64_t* steps = calloc((size_t)2 * nconn, sizeof(uint64_t)); /* per channel and ring index: send, recv */
+  uint8_t* pin = malloc(g.step_bytes);
+  uint8_t* pout = malloc(g.step_bytes);
+  float* vals = malloc(sizeof(float) * (g.chunk_elems + 64));
+  slice_t* prog[MAXR] = {0};
+  size_t cursor[MAXR];
+  int64_t sends[MAXR], recvs[MAXR];
+  int rc = ORC_OK;
+  sim_t S;
+  memset(&S, 0, sizeof S);
+  if (!conn || !fifo || !wstep || !acc || !pbuf || !steps || !pin || !pout || !vals) { rc = ORC_ENOMEM; goto done; }
+  for (size_t k = 0; k < nconn * NSTEPS * slines; k++) wstep[k] = NEVER;
+  for (size_t e = 0; e < nconn; e++) {
+    conn[e].fifo = fifo + e * NSTEPS * g.step_bytes;
+    conn[e].wstep = wstep + e * NSTEPS * slines;
+    conn[e].acc = acc + e * slines;
+    conn[e].pbuf = pbuf + e * slines * 8;
+  }
+  S.g = &g;
+  S.rank_at = rank_at;
+  S.sends = sends;
+  S.recvs = recvs;
+  S.pay_in = pin;
+  S.pay_out = pout;
+  S.vals = vals;
+  S.session = 1;
+  S.flag_max = flag_max;
+  S.cleanup = cleanup;
+  for (int k = 0; k < ncalls; k++) {
+    g.count = counts[k];
+    g.per_channel = align_up(div_up(g.count, (size_t)g.nchan), g.align_elems);
+    S.send = send + (size_t)k * nranks;
+    S.recv = recv + (size_t)k * nranks;
+    if (g.count == 0) continue; /* an empty call advances nothing */
+    for (int ch = 0; ch < g.nchan; ch++) {
+      rank_at_index(nranks, ring_order + (nrings == 1 ? 0 : (size_t)ch * nranks), rank_at);
+      size_t gridOffset, channelCount;
+      channel_range(&g, ch, &gridOffset, &channelCount);
+      S.conn = conn + (size_t)ch * nranks;
+      size_t nslices = 0;
+      for (int i = 0; i < nranks; i++) {
+        S.sstep[i] = steps[2 * ((size_t)ch * nranks + i)];
+        S.rstep[i] = steps[2 * ((size_t)ch * nranks + i) + 1];
+        nslices = build_program(&g, rank_at, i, gridOffset, channelCount, NULL);
+        free(prog[i]);
+        prog[i] = malloc(sizeof(slice_t) * (nslices ? nslices : 1));
+        if (!prog[i]) { rc = ORC_ENOMEM; goto done; }
+        build_program(&g, rank_at, i, gridOffset, channelCount, prog[i]);
+        cursor[i] = 0;
+      }
+      int finished = 0;
+      while (finished < nranks && nslices > 0) {
+        int progressed = 0;
+        for (int i = 0; i < nranks; i++) {
+          while (cursor[i] < nslices) {
+            int r = sim_try_slice(&S, i, &prog[i][cursor[i]]);
+            if (r < 0) { rc = -r; goto done; }
+            if (r == 0) break;
+            cursor[i]++;
+            progressed = 1;
+            if (cursor[i] == nslices) finished++;
+          }
+        }
+        if (!progressed) { rc = ORC_EDEADLOCK; goto done; }
+      }
+      for (int i = 0; i < nranks; i++) {
+        steps[2 * ((size_t)ch * nranks + i)] = S.sstep[i];
+        steps[2 * ((size_t)ch * nranks + i) + 1] = S.rstep[i];
+      }
+    }
+  }
+done:
+  if (stale_accepts) *stale_accepts = S.stale_accepts;
+  if (max_stale_age) *max_stale_age = S.max_stale_age;
+  for (int i = 0; i < nranks; i++) free(prog[i]);
+  free(conn);
+  free(fifo);
+  free(wstep);
+  free(acc);
+  free(pbuf);
+  free(steps);
+  free(pin);
+  free(pout);
+  free(vals);
+  return rc;
 }
 
 /* ------------------------------------------------------------------ */
