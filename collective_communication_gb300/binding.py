@@ -43,6 +43,7 @@ EXPORTED = (
     "rar_strerror", "rar_set_spin_timeout_ns", "rar_debug_set_fault", "rar_describe_geometry",
     "rar_allreduce_static", "rar_allreduce_ex", "rar_reduce_scatter", "rar_all_gather",
     "rar_oneshot_workspace_bytes", "rar_oneshot_workspace_init", "rar_oneshot_staged",
+    "rar_debug_set_ll_flag_wrap",
 )
 
 
@@ -99,6 +100,8 @@ def load_library():
     L.rar_oneshot_workspace_init.restype = I
     L.rar_oneshot_staged.argtypes = [P, P, I, SZ, I, I, P, SZ, P]
     L.rar_oneshot_staged.restype = I
+    L.rar_debug_set_ll_flag_wrap.argtypes = [ctypes.c_uint32]
+    L.rar_debug_set_ll_flag_wrap.restype = I
     _lib = L
     return L
 
@@ -298,6 +301,12 @@ def set_spin_timeout_ns(ns: int) -> None:
 
 def debug_set_fault(fault: int) -> None:
     load_library().rar_debug_set_fault(fault)
+
+
+def debug_set_ll_flag_wrap(flag_max: int) -> None:
+    """LL flag test mode: 0 = production flags, else the wrap period (a power
+    of two >= 64) with the slot cleanup."""
+    _check(load_library().rar_debug_set_ll_flag_wrap(flag_max), "rar_debug_set_ll_flag_wrap")
 
 
 def describe_geometry(nranks, count, dtype, mask, proto, buff_size=0, chunk_steps=4):

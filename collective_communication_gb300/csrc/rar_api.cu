@@ -19,6 +19,7 @@ namespace {
 
 std::atomic<uint64_t> g_timeout_ns{0};
 std::atomic<int> g_fault{0};
+std::atomic<uint32_t> g_ll_flag_max{0};
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
@@ -227,6 +228,7 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
   a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
   a.timeout_ns = spin_timeout_ns();
   a.fault = g_fault.load(std::memory_order_relaxed);
+  a.ll_flag_max = g.proto == kLL ? g_ll_flag_max.load(std::memory_order_relaxed) : 0u;
   a.direct = direct ? 1 : 0;
   const int grid = nranks * g.nchan;
   cudaStream_t s = (cudaStream_t)stream;
@@ -413,6 +415,13 @@ const char* rar_strerror(rar_status status) {
 void rar_set_spin_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns, std::memory_order_relaxed); }
 
 void rar_debug_set_fault(int fault) { g_fault.store(fault, std::memory_order_relaxed); }
+
+rar_status rar_debug_set_ll_flag_wrap(uint32_t flag_max) {
+  if (flag_max != 0 && (flag_max < 64 || flag_max > (1u << 31) || (flag_max & (flag_max - 1)) != 0))
+    return RAR_ERR_ARG;
+  g_ll_flag_max.store(flag_max, std::memory_order_relaxed);
+  return RAR_OK;
+}
 
 rar_status rar_describe_geometry(int nranks, size_t count, rar_dtype dtype, uint64_t channelMask, rar_proto proto,
                                  size_t buffSize, int chunkSteps, int64_t* out) {

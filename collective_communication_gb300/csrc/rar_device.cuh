@@ -83,6 +83,7 @@ struct RingArgs {
   int64_t fifo_offset;         // byte offset of the FIFO array
   uint64_t timeout_ns;
   int fault;
+  uint32_t ll_flag_max;        // LL: 0 = flag step + 1 (32 bits); else flags wrap at this power of two
 };
 
 // ---------------------------------------------------------------------------
@@ -317,6 +318,21 @@ __device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* den
 __device__ __forceinline__ int ring_index_of(const RingArgs& a, int dense, int rank) {
   return a.ring_index[dense * kMaxRanks + rank];
 }
+// LL flag of a step ([C23] "LL：Data 与 Flag 同 Line"): step + 1, or, in the
+// wrap test mode, step + 1 modulo the power of two ll_flag_max.
+__device__ __forceinline__ uint32_t ll_flag(const RingArgs& a, uint64_t step) {
+  return a.ll_flag_max ? (uint32_t)((step + 1) & (uint64_t)(a.ll_flag_max - 1)) : (uint32_t)(step + 1);
+}
+// Wrap mode: on the last NCCL_STEPS steps of every half flag period (once per
+// slot every ll_flag_max / 2 steps) the sender rewrites every line of its slot
+// past its slice with the current flag, so that no line is ever older than
+// half a period when it is read and none can carry a later step's flag.
+__device__ __forceinline__ bool ll_cleanup_step(const RingArgs& a, uint64_t step) {
+  if (a.ll_flag_max == 0) return false;
+  const uint64_t half = a.ll_flag_max / 2;
+  return step % half >= half - kSteps;
+}
+
 __device__ __forceinline__ int rank_at_index(const RingArgs& a, int dense, int ring_idx) {
   return a.ring_rank[dense * kMaxRanks + ring_idx];
 }

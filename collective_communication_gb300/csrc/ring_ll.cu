@@ -152,8 +152,8 @@ __device__ __forceinline__ bool ll_poll(const RingArgs& a, const char* p, uint32
 
 template <typename T, int PRIM, int NT>
 __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out, const char* rslot, char* sslot,
-                                         int64_t nelem, uint32_t rflag, uint32_t sflag, volatile int* sh_abort,
-                                         uint64_t info) {
+                                         int64_t nelem, uint32_t rflag, uint32_t sflag, bool clean,
+                                         volatile int* sh_abort, uint64_t info) {
   constexpr int K = LLUnit<T>::kElems;
   constexpr int PL = LLUnit<T>::kPartLines;
   constexpr int UL = 1;
@@ -232,6 +232,13 @@ __device__ __forceinline__ void ll_slice(const RingArgs& a, const T* in, T* out,
         if (kSendFinal) st_line_v4(sslot + unit * 16, make_uint4(f.x, sflag, f.y, sflag));
       }
     }
+  }
+  // flag-wrap mode: the rest of the slot gets the current flag (no payload)
+  if ((kSendPartial || kSendFinal) && clean) {
+    const int64_t sent = nunits * (kSendPartial ? PL : 1);
+    const int64_t slot_lines = a.geo.step_bytes / 16;
+    for (int64_t l = sent + threadIdx.x; l < slot_lines; l += NT)
+      st_line_v4(sslot + l * 16, make_uint4(0u, sflag, 0u, sflag));
   }
 }
 
@@ -437,7 +444,7 @@ __device__ __noinline__ bool pace_wait(const RingArgs& a, const char* rslot, int
     if (nunits <= NT) return true;
     const int64_t lines = nunits * (partial ? LLUnit<T>::kPartLines : 1);
     const char* p = rslot + (lines - 1) * 16;
-    const uint32_t flag = (uint32_t)(rstep + 1);
+    const uint32_t flag = ll_flag(a, rstep);
     uint4 v = ld_line_v4(p);
     while (!ll_ready(v, flag)) {
       if (sp.poll(a, info, flag)) return false;
@@ -463,15 +470,24 @@ __device__ __forceinline__ void line_slice(int prim, const RingArgs& a, const T*
                                            char* sslot, int64_t nelem, uint64_t rstep, uint64_t sstep,
                                            volatile int* sh_abort, uint64_t info, uint16_t* stage) {
   if (PROTO == kLL) {
-    const uint32_t rf = (uint32_t)(rstep + 1), sf = (uint32_t)(sstep + 1);
+    const uint32_t rf = ll_flag(a, rstep), sf = ll_flag(a, sstep);
+    const bool clean = ll_cleanup_step(a, sstep);
     switch (prim) {
-      case kSend: ll_slice<T, kSend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      case kRecvReduceSend: ll_slice<T, kRecvReduceSend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      case kRecvReduceCopySend: ll_slice<T, kRecvReduceCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      case kRecvCopySend: ll_slice<T, kRecvCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      case kRecvReduceCopy: ll_slice<T, kRecvReduceCopy, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      case kCopySend: ll_slice<T, kCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
-      default: ll_slice<T, kRecv, NT>(a, in, out, rslot, sslot, nelem, rf, sf, sh_abort, info); break;
+      case kSend: ll_slice<T, kSend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info); break;
+      case kRecvReduceSend:
+        ll_slice<T, kRecvReduceSend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info);
+        break;
+      case kRecvReduceCopySend:
+        ll_slice<T, kRecvReduceCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info);
+        break;
+      case kRecvCopySend:
+        ll_slice<T, kRecvCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info);
+        break;
+      case kRecvReduceCopy:
+        ll_slice<T, kRecvReduceCopy, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info);
+        break;
+      case kCopySend: ll_slice<T, kCopySend, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info); break;
+      default: ll_slice<T, kRecv, NT>(a, in, out, rslot, sslot, nelem, rf, sf, clean, sh_abort, info); break;
     }
   } else {
     const uint64_t rf = rstep + 1, sf = sstep + 1;

@@ -340,6 +340,21 @@ RAR_API void rar_set_spin_timeout_ns(uint64_t ns);
 RAR_API void rar_debug_set_fault(int fault);
 
 /*
+ * Test mode of the LL flags ([C23] "LL：Data 与 Flag 同 Line": a test macro
+ * makes the flag wrap at 0x100, and a cleanup keeps the wrap correct).
+ * flag_max 0 (default): the production flag, step + 1 as 32 bits. A power of
+ * two in [64, 2^31]: LL flags are (step + 1) mod flag_max, and on the last
+ * RAR_NCCL_STEPS steps of every flag_max / 2 steps a sender also rewrites
+ * every line of its FIFO slot past its slice with the current flag, so no
+ * line is ever older than half a period when it is read and none can carry
+ * the flag of a later step. Results are unchanged. Applies to LL launches
+ * enqueued after the call; a workspace used under one mode must be
+ * re-initialised (rar_workspace_init) before calls under the other. Returns
+ * RAR_ERR_ARG (and changes nothing) for any other flag_max.
+ */
+RAR_API rar_status rar_debug_set_ll_flag_wrap(uint32_t flag_max);
+
+/*
  * The geometry a ring AllReduce call would use, computed on the host with
  * no device work (the "TRACE" view of [C23] "Kernel 如何把 Block 映射到
  * Channel" and [C12] "runRing 的数据切分"). out receives, in order:

@@ -264,3 +264,12 @@ def test_staged_oneshot_argument_errors(lib):
     assert L.rar_oneshot_workspace_init(FAKE + 16, 1 << 30, 4, 1024, 0, None) == S.ERR_ALIGN
     assert L.rar_oneshot_workspace_init(FAKE, 4096, 4, 1024, 0, None) == S.ERR_WORKSPACE
     assert L.rar_oneshot_workspace_init(FAKE, 1 << 30, 0, 1024, 0, None) == S.ERR_ARG
+
+
+def test_ll_flag_wrap_setter(lib):
+    L = B.load_library()
+    S = B.Status
+    for bad in (1, 63, 96, 255, 257, 1 << 32 - 1 | 1):
+        assert L.rar_debug_set_ll_flag_wrap(bad) == S.ERR_ARG
+    for good in (64, 256, 1 << 20, 1 << 31, 0):
+        assert L.rar_debug_set_ll_flag_wrap(good) == S.OK
