@@ -34,9 +34,10 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# headline kernel from one ncu capture of this workload; None until measured
-# for the current kernel (see profiles/).
-TRAFFIC_BYTES_PER_LAUNCH = None
+# headline kernel from one ncu capture of this workload, for the kernel as it
+# is now (profiles/ring_simple_f32_n8_64MiB_traffic.md); None whenever the
+# kernel changes until it is captured again.
+TRAFFIC_BYTES_PER_LAUNCH = 1789532928
 
 
 def headline_case(args=None):
