@@ -539,7 +539,13 @@ def run_gpu(args):
     ms_per_step, value = combine_replicas(total_ms, args.steps, case.bytes_per_rank, case.nranks, world,
                                           dist if world > 1 else None, "cuda")
     avg_launch = statistics.mean(launch_ms) / 1e3
+    cv = statistics.pstdev(launch_ms) / statistics.mean(launch_ms) if len(launch_ms) > 1 else 0.0
     algo = algorithmic_bytes(case)
+    default_case = headline_case(None)
+    is_headline = (case.nranks, case.count, case.mask, case.proto, case.buff_size) == (
+        default_case.nranks, default_case.count, default_case.mask, default_case.proto, default_case.buff_size)
+    kernel = {"Simple": "ring_simple_kernel<float>", "LL": "ring_line_kernel<float, LL>",
+              "LL128": "ring_ll128_bulk_kernel<float> (ring_line_kernel<float, LL128> for chunks < 3840)"}[case.proto]
     achieved = algo / avg_launch / 1e9
     del x, y, ws
     torch.cuda.empty_cache()
@@ -554,7 +560,8 @@ def run_gpu(args):
         return
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "cv_per_step": round(cv, 4),
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"ring AllReduce, {case.nranks} virtual ranks on one GPU, f32 sum, "
                                f"{case.bytes_per_rank >> 20} MiB per rank, ring = seeded permutation (seed 3), "
@@ -566,8 +573,10 @@ def run_gpu(args):
                    "l2": f"inputs larger than L2 ({case.nranks} x {case.bytes_per_rank >> 20} MiB in and out per step)",
                    "parallelism": f"replicas x{world} (no GPU-to-GPU data path)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 3), "traffic": TRAFFIC_BYTES_PER_LAUNCH,
-                     "kernel": "ring_simple_kernel<float>" if case.proto == "Simple" else "ring_line_kernel<float>",
+                     "frac": round(achieved / peak, 3),
+                     # the captured traffic belongs to the headline workload only
+                     "traffic": TRAFFIC_BYTES_PER_LAUNCH if is_headline else None,
+                     "kernel": kernel,
                      "algorithmic_bytes_per_launch": int(algo),
                      "peak_kind": f"{peak_kind} copy peak (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
