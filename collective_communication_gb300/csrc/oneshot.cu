@@ -9,8 +9,10 @@
 //
 // On one GPU the ranks' buffers are already addressable by pointer, so the
 // copy-in / signal / wait stages of the page's kernel have nothing to move or
-// wait for: the N inputs are read directly, and since every rank's result is
-// the same sum, each pack is reduced once and written to all N outputs.
+// wait for: each rank's blocks read the N inputs directly. Block b serves
+// rank b % N and tile b / N; the N blocks of a tile are adjacent in launch
+// order, so they run together and the N-fold reads of one input tile are
+// served mostly from L2.
 //
 // Sum: binary32, in user-rank order 0..N-1, starting from x_0 (no added
 // zero), rounded once to bf16 for bf16 data.
@@ -19,6 +21,7 @@
 namespace rar {
 
 constexpr int kOneShotThreads = 256;
+constexpr int kOneShotUnroll = 1;  // low register count: more resident warps per SM
 
 template <typename T>
 struct OsPack;
@@ -62,51 +65,70 @@ __device__ __forceinline__ void os_store_scalar<uint16_t>(uint16_t* p, float v) 
   *p = *reinterpret_cast<uint16_t*>(&b);
 }
 
-// Every rank's result is the same value, so each 16-byte pack is reduced
-// once and stored to all N outputs (the N ranks' blocks of the page's kernel
-// would each read all N inputs: N times the reads for the same sums). Peers
-// are read in batches of kBatch ranks: every load of a batch is issued before
-// any is added, so a thread keeps kBatch 16-byte loads in flight; the
-// additions then run strictly in rank order.
+// Peers are read in batches of kBatch ranks: every load of a batch is issued
+// before any is added, so a thread keeps kBatch x U 16-byte loads in flight;
+// the additions then run strictly in rank order.
 constexpr int kBatch = 8;
 
 template <typename T>
 __global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_constant__ OneShotArgs a) {
   constexpr int P = OsPack<T>::kElems;
+  constexpr int U = kOneShotUnroll;
   const int N = a.nranks;
+  const int rank = blockIdx.x % N;
+  const int64_t tile = blockIdx.x / N;
+  const int64_t ntiles = gridDim.x / N;
   const int64_t npack = a.count / P;
-  const int64_t stride = (int64_t)gridDim.x * kOneShotThreads;
-  for (int64_t p = (int64_t)blockIdx.x * kOneShotThreads + threadIdx.x; p < npack; p += stride) {
-    float acc[8];
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
+  const int64_t per_tile = (int64_t)kOneShotThreads * U;
+  for (int64_t base = tile * per_tile; base < npack; base += ntiles * per_tile) {
+    float acc[U][8];
     for (int q0 = 0; q0 < N; q0 += kBatch) {
-      uint4 w[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; b++)
-        if (q0 + b < N) w[b] = ld_stream_v4(reinterpret_cast<const T*>(a.send[q0 + b]) + p * P);
+      uint4 w[kBatch][U];
 #pragma unroll
       for (int b = 0; b < kBatch; b++) {
         if (q0 + b < N) {
-          float v[8];
-          OsPack<T>::widen(w[b], v);
-          if (q0 + b == 0) {
+          const T* src = reinterpret_cast<const T*>(a.send[q0 + b]);
 #pragma unroll
-            for (int j = 0; j < P; j++) acc[j] = v[j];  // the sum starts at x_0
-          } else {
+          for (int u = 0; u < U; u++) {
+            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+            if (p < npack) w[b][u] = ld_stream_v4(src + p * P);
+          }
+        }
+      }
 #pragma unroll
-            for (int j = 0; j < P; j++) acc[j] = __fadd_rn(acc[j], v[j]);
+      for (int b = 0; b < kBatch; b++) {
+        if (q0 + b < N) {
+#pragma unroll
+          for (int u = 0; u < U; u++) {
+            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+            if (p < npack) {
+              float v[8];
+              OsPack<T>::widen(w[b][u], v);
+              if (q0 + b == 0) {
+#pragma unroll
+                for (int j = 0; j < P; j++) acc[u][j] = v[j];  // the sum starts at x_0
+              } else {
+#pragma unroll
+                for (int j = 0; j < P; j++) acc[u][j] = __fadd_rn(acc[u][j], v[j]);
+              }
+            }
           }
         }
       }
     }
-    const uint4 r = OsPack<T>::narrow(acc);
-    for (int q = 0; q < N; q++) st_v4(reinterpret_cast<T*>(a.recv[q]) + p * P, r);
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+      const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
+      if (p < npack) st_v4(out + p * P, OsPack<T>::narrow(acc[u]));
+    }
   }
-  // ragged end (fewer than one 16-byte pack): block 0
-  if (blockIdx.x == 0) {
+  // ragged end (fewer than one 16-byte pack): tile 0 of each rank
+  if (tile == 0) {
     for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kOneShotThreads) {
       float acc = os_scalar<T>(reinterpret_cast<const T*>(a.send[0]) + e);
       for (int q = 1; q < N; q++) acc = __fadd_rn(acc, os_scalar<T>(reinterpret_cast<const T*>(a.send[q]) + e));
-      for (int q = 0; q < N; q++) os_store_scalar<T>(reinterpret_cast<T*>(a.recv[q]) + e, acc);
+      os_store_scalar<T>(out + e, acc);
     }
   }
 }
@@ -126,12 +148,13 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
-  // enough blocks to fill every SM several times over, never more than needed
-  int64_t blocks = div_up(npack, kOneShotThreads);
-  const int64_t cap = (int64_t)sms * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  cfg.gridDim = dim3((unsigned)blocks);
+  const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;
+  // enough tiles to fill every SM several times over, never more than needed
+  int64_t tiles = div_up(npack, per_tile);
+  const int64_t cap = div_up((int64_t)sms * 8, a.nranks);
+  if (tiles > cap) tiles = cap;
+  if (tiles < 1) tiles = 1;
+  cfg.gridDim = dim3((unsigned)(tiles * a.nranks));
   cfg.blockDim = dim3(kOneShotThreads);
   if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_kernel<float>, a);
   return cudaLaunchKernelEx(&cfg, oneshot_kernel<uint16_t>, a);

@@ -23,14 +23,10 @@
 //   signal   fence, atomicAdd(done[r], 1); the block that gets (G-1) mod G
 //            publishes tx_seq[r] = s + 1 (release).
 //   wait     every block waits until tx_seq[q] >= s + 1 for all q (acquire).
-//   reduce   T(sum over q = 0..N-1 of slot (q, s % RING)), binary32, in user-rank
-//            order, rounded once for bf16: the same for every rank, so each
-//            pack is reduced once (by any of the N*G blocks) and stored to all
-//            N outputs.
-//   ack      fence, atomicAdd(read[r], 1); the last block of the G blocks
-//            numbered with rank r publishes ack_seq[r] = s + 1. Once every
-//            rank has acknowledged call s, every block has finished reading
-//            call s's slots.
+//   reduce   out_r = T(sum over q = 0..N-1 of slot (q, s % RING)), binary32, in
+//            user-rank order, rounded once for bf16.
+//   ack      fence, atomicAdd(read[r], 1); the last block publishes
+//            ack_seq[r] = s + 1: rank r has finished reading call s's slots.
 // A block reads tx_seq before its own atomicAdd, and the block that publishes
 // s + 1 exists only after every block of the launch has added, so no block of
 // this launch can read s + 1 at entry. All N*G blocks wait on each other, so
@@ -163,10 +159,8 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   if (sh_stop) return;
 
   // ---- reduce the N staged copies, in user-rank order ----
-  // Every rank's result is the same sum, so the packs are spread over all
-  // N*G blocks and each is reduced once and stored to all N outputs.
-  const int64_t stride = (int64_t)N * G * kStagedThreads;
-  for (int64_t p = (int64_t)blockIdx.x * kStagedThreads + threadIdx.x; p < npack; p += stride) {
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
+  for (int64_t p = (int64_t)j * kStagedThreads + threadIdx.x; p < npack; p += (int64_t)G * kStagedThreads) {
     float acc[8];
     for (int q0 = 0; q0 < N; q0 += kBatchRanks) {
       uint4 w[kBatchRanks];
@@ -188,14 +182,13 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
         }
       }
     }
-    const uint4 r = StPack<T>::narrow(acc);
-    for (int q = 0; q < N; q++) st_v4(reinterpret_cast<T*>(a.recv[q]) + p * P, r);
+    st_v4(out + p * P, StPack<T>::narrow(acc));
   }
-  if (blockIdx.x == 0) {
+  if (j == 0) {
     for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kStagedThreads) {
       float acc = StPack<T>::scalar(os_slot(a, sb, 0, s) + e * (int64_t)sizeof(T));
       for (int q = 1; q < N; q++) acc = __fadd_rn(acc, StPack<T>::scalar(os_slot(a, sb, q, s) + e * (int64_t)sizeof(T)));
-      for (int q = 0; q < N; q++) StPack<T>::store_scalar(reinterpret_cast<T*>(a.recv[q]) + e, acc);
+      StPack<T>::store_scalar(out + e, acc);
     }
   }
   __syncthreads();
