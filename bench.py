@@ -278,26 +278,25 @@ def sweep(torch, B, steps, warmup, peak):
         ms = time_ring(c, torch, B, max(steps, 20), warmup)
         out[f"n4_{proto}_ch1_4KiB"] = {"stream_latency_us": round(statistics.median(ms) * 1e3, 2),
                                        "graph_latency_us": graph_latency_ring(c, torch, B)}
-    # busBW and roofline fraction vs size per protocol: N=8, seeded ring (seed
-    # 5), the sparse 8-channel mask 0b101101011011, f32, 1 KiB * 4^k per rank
-    # up to 1 GiB; small sizes timed from a CUDA graph (device time only)
+    # busBW and roofline fraction vs size per protocol and type: N=8, seeded
+    # ring (seed 5), the sparse 8-channel mask 0b101101011011, 1 KiB * 4^k per
+    # rank up to 1 GiB with the uneven counts 8 * chunk * k + 13 of that
+    # workload; small sizes timed from a CUDA graph (device time only)
+    def chunk_elems_of(proto, dtype):
+        dt = B.Dtype.F32 if dtype == gen.F32 else B.Dtype.BF16
+        return B.describe_geometry(8, 1 << 20, dt, gen.SPARSE_MASK, proto, 0, 4)["chunk_elems"]
+
     sizes = {}
-    for proto in ("LL", "LL128", "Simple"):
-        row = {}
-        size = gen.KIB
-        while size <= (1 << 30):
-            c = gen.RingCase(f"sweep_{proto}_{size}", 8, gen.ring_permutation(8, 5), gen.SPARSE_MASK, proto,
-                             size // 4, gen.F32, "normal", 5, 0, 4)
-            if size <= 4 * gen.MIB:
-                t = graph_latency_ring(c, torch, B) / 1e6
-            else:
-                t = statistics.median(time_ring(c, torch, B, 3 if size >= 256 * gen.MIB else 5, 2)) / 1e3
-            row[f"{size // gen.KIB}KiB"] = {"busbw_gbs": round(busbw(c.bytes_per_rank, 8, t), 2),
-                                           "us": round(t * 1e6, 2),
-                                           "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
-            size *= 4
-        sizes[proto] = row
-    out["size_sweep_n8_sparse_mask_f32_default_buffers"] = sizes
+    for c in gen.sparse_sweep_cases(chunk_elems_of, max_bytes=1 << 30):
+        label = c.name.rsplit("_", 1)[1]  # the nominal size per rank
+        if c.bytes_per_rank <= 4 * gen.MIB:
+            t = graph_latency_ring(c, torch, B) / 1e6
+        else:
+            t = statistics.median(time_ring(c, torch, B, 3 if c.bytes_per_rank >= 256 * gen.MIB else 5, 2)) / 1e3
+        sizes.setdefault(c.dtype, {}).setdefault(c.proto, {})[label] = {
+            "count": c.count, "busbw_gbs": round(busbw(c.bytes_per_rank, 8, t), 2), "us": round(t * 1e6, 2),
+            "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
+    out["size_sweep_n8_sparse_mask_default_buffers"] = sizes
     # one-shot bf16, N=8, 7168 x {1, 512}
     for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
         x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
