@@ -164,19 +164,30 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def rows_like(x, torch):
+    """An uninitialised [nranks, count] tensor like x whose rows start on
+    256-byte boundaries (the ABI wants 16-byte aligned rank buffers; a ragged
+    count would misalign every row after the first in a dense tensor)."""
+    n, count = x.shape
+    stride = -(-count // 128) * 128
+    return torch.empty((n, stride), dtype=x.dtype, device=x.device)[:, :count]
+
+
 def device_inputs(case, torch):
     g = torch.Generator(device="cuda")
     g.manual_seed(case.seed)
     x = torch.randn((case.nranks, case.count), generator=g, device="cuda", dtype=torch.float32)
     if case.dtype == "bf16":
         x = x.to(torch.bfloat16)
-    return x
+    y = rows_like(x, torch)
+    y.copy_(x)
+    return y
 
 
 def time_ring(case, torch, B, steps, warmup, direct=False):
     """Device time per call (CUDA events on the launching stream)."""
     x = device_inputs(case, torch)
-    y = torch.empty_like(x)
+    y = rows_like(x, torch)
     send = [x[r] for r in range(case.nranks)]
     recv = [y[r] for r in range(case.nranks)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
@@ -301,7 +312,7 @@ def sweep(torch, B, steps, warmup, peak):
     for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
         x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
                                        case.seed), torch)
-        y = torch.empty_like(x)
+        y = rows_like(x, torch)
         send = [x[r] for r in range(case.nranks)]
         recv = [y[r] for r in range(case.nranks)]
         for _ in range(warmup):
@@ -374,7 +385,7 @@ def graph_latency(call, torch, reps=50):
 
 def graph_latency_ring(case, torch, B):
     x = device_inputs(case, torch)
-    y = torch.empty_like(x)
+    y = rows_like(x, torch)
     send = [x[r] for r in range(case.nranks)]
     recv = [y[r] for r in range(case.nranks)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
@@ -396,8 +407,8 @@ def e2e_ring(case, torch, B, steps, warmup):
     x = device_inputs(case, torch)
     host_in = x.cpu().pin_memory()
     host_out = [torch.empty_like(host_in).pin_memory() for _ in range(2)]
-    dx = [torch.empty_like(x) for _ in range(2)]
-    dy = [torch.empty_like(x) for _ in range(2)]
+    dx = [rows_like(x, torch) for _ in range(2)]
+    dy = [rows_like(x, torch) for _ in range(2)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
     s_h2d, s_cmp, s_d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
@@ -503,7 +514,7 @@ def run_gpu(args):
     case = headline_case(args)
 
     x = device_inputs(case, torch)
-    y = torch.empty_like(x)
+    y = rows_like(x, torch)
     send = [x[r] for r in range(case.nranks)]
     recv = [y[r] for r in range(case.nranks)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
@@ -604,7 +615,7 @@ def run_oneshot_only(args):
     g = torch.Generator(device="cuda")
     g.manual_seed(case.seed)
     x = torch.randn((8, case.count), generator=g, device="cuda").to(torch.bfloat16)
-    y = torch.empty_like(x)
+    y = rows_like(x, torch)
     send = [x[r] for r in range(8)]
     recv = [y[r] for r in range(8)]
     for _ in range(args.warmup):
