@@ -605,7 +605,8 @@ def run_gpu(args):
 
 def run_oneshot_only(args):
     """Time only the one-shot AllReduce: N=8 bf16 ranks, 7168 x T elements each
-    (T = --oneshot-tokens), CUDA events around each call, one JSON line."""
+    (T = --oneshot-tokens), CUDA events around each call, one JSON line.
+    --oneshot-staged times the staged form instead of the direct one."""
     import torch
     from collective_communication_gb300 import binding as B
     from collective_communication_gb300 import inputs as gen
@@ -618,21 +619,29 @@ def run_oneshot_only(args):
     y = rows_like(x, torch)
     send = [x[r] for r in range(8)]
     recv = [y[r] for r in range(8)]
+    if args.oneshot_staged:
+        ws = B.OneShotWorkspace(8, case.count, "bf16")
+        call = lambda: B.oneshot_staged(send, recv, ws)  # noqa: E731
+    else:
+        call = lambda: B.oneshot(send, recv)  # noqa: E731
     for _ in range(args.warmup):
-        B.oneshot(send, recv)
+        call()
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for a, b in ev:
         a.record(s)
-        B.oneshot(send, recv)
+        call()
         b.record(s)
     torch.cuda.synchronize()
+    if args.oneshot_staged and B.get_status(ws) != B.Status.OK:
+        raise RuntimeError("staged one-shot: device status not OK")
     t = statistics.median([a.elapsed_time(b) for a, b in ev]) / 1e3
-    unique = 2 * 8 * case.count * 2
+    # unique bytes: inputs read and outputs written once (the staged form adds its copy)
+    unique = (4 if args.oneshot_staged else 2) * 8 * case.count * 2
     print(json.dumps({"metric": "one-shot AllReduce time", "value": round(t * 1e6, 2), "unit": "us",
                       "higher_is_better": False, "steps": args.steps, "warmup": args.warmup, "dtype": "bf16",
-                      "config": {"workload": case.name},
+                      "config": {"workload": case.name + ("_staged" if args.oneshot_staged else "")},
                       "unique_bytes_frac": round(unique / t / 1e9 / peak, 3)}))
 
 
@@ -689,6 +698,7 @@ def main():
     ap.add_argument("--nranks", type=int)
     ap.add_argument("--channels", type=int)
     ap.add_argument("--oneshot-tokens", type=int, help="time only the one-shot AllReduce of 7168 x T bf16")
+    ap.add_argument("--oneshot-staged", action="store_true", help="with --oneshot-tokens: the staged form")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

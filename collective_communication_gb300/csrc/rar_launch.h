@@ -26,7 +26,7 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream);
 // then kStagingSlots slots of slot_bytes per rank.
 constexpr uint32_t kStagedMagic = 0x31534152u;  // "RAS1"
 constexpr int kStagingSlots = 4;                // slots per rank, reused round-robin
-constexpr int kStagedBlocksPerSm = 2;           // grid = nranks * (SMs * 2 / nranks) blocks
+constexpr int kStagedBlocksPerSm = 4;           // grid = nranks * (SMs * 4 / nranks) blocks
 
 struct OsHeader {
   uint32_t magic;

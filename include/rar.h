@@ -248,7 +248,7 @@ RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbuf
  *   max_count elements of dtype over nranks ranks (0 for invalid arguments):
  *   a 4 KiB header, 512 B of counters per rank, 4 slots per rank.
  * rar_oneshot_workspace_init: zero the header and counters, record the
- *   configuration (nranks, dtype, max_count, and the grid, 2 * SMs / nranks
+ *   configuration (nranks, dtype, max_count, and the grid, 4 * SMs / nranks
  *   blocks per rank on the current device); enqueued on `stream`. Errors:
  *   RAR_ERR_ARG, RAR_ERR_WORKSPACE (null or too small), RAR_ERR_ALIGN (not
  *   256-byte aligned), RAR_ERR_CUDA.
