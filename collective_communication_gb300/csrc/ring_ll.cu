@@ -532,10 +532,12 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   char* fifo_send = fifo_at(a, dense, e_send);
   const char* fifo_recv = fifo_at(a, dense, e_recv);
   if (threadIdx.x == 0) {
+    // Both counters belong to this block and equal the previous call's final
+    // step; they are read together with the header (one round trip, not two).
+    const uint64_t tail0 = ld_relaxed_u64(&cs->tail), head0 = ld_relaxed_u64(&cr->head);
     sh_abort = entry_check(a) ? 0 : 1;
-    // Both counters belong to this block and equal the previous call's final step.
-    sh_base_send = ld_relaxed_u64(&cs->tail);
-    sh_base_recv = ld_relaxed_u64(&cr->head);
+    sh_base_send = tail0;
+    sh_base_recv = head0;
     reinterpret_cast<uint8_t*>(a.ws + kTraceOffset)[blockIdx.x] = (uint8_t)sh_chan;
   }
   __syncthreads();
@@ -887,6 +889,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
   char* fifo_send = fifo_at(a, dense, e_send);
   const char* fifo_recv = fifo_at(a, dense, e_recv);
   if (threadIdx.x == 0) {
+    const uint64_t tail0 = ld_relaxed_u64(&cs->tail), head0 = ld_relaxed_u64(&cr->head);  // with the header
     sh_abort = entry_check(a) ? 0 : 1;
     for (int d = 0; d < kL8Depth; d++) {
       mbar_init(&bar_ready[d], 1);
@@ -899,8 +902,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
     }
     mbar_init(&bar_fin, kL8Warps);
     // Both counters belong to this block and equal the previous call's final step.
-    sh_base_send = ld_relaxed_u64(&cs->tail);
-    sh_base_recv = ld_relaxed_u64(&cr->head);
+    sh_base_send = tail0;
+    sh_base_recv = head0;
     reinterpret_cast<uint8_t*>(a.ws + kTraceOffset)[blockIdx.x] = (uint8_t)sh_chan;
   }
   __syncthreads();

@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   const char* fifo_recv = fifo_at(a, dense, e_recv);
 
   if (threadIdx.x == 0) {
+    const uint64_t tail0 = ld_relaxed_u64(&cs->tail), head0 = ld_relaxed_u64(&cr->head);  // with the header
     sh_abort = entry_check(a) ? 0 : 1;
     for (int d = 0; d < kDepth; d++) {
       mbar_init(&bar_ready[d], 1);
@@ -344,8 +345,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
     // This block alone writes the tail of its send edge and the head of its
     // receive edge; both equal the previous call's final step. Slices start
     // on a multiple of NCCL_STEPS so that no slice wraps around the ring.
-    sh_base_send = round_up_steps(ld_relaxed_u64(&cs->tail));
-    sh_base_recv = round_up_steps(ld_relaxed_u64(&cr->head));
+    sh_base_send = round_up_steps(tail0);
+    sh_base_recv = round_up_steps(head0);
     reinterpret_cast<uint8_t*>(a.ws + kTraceOffset)[blockIdx.x] = (uint8_t)sh_chan;
   }
   __syncthreads();
