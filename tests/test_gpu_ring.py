@@ -300,3 +300,44 @@ def test_dropped_head_times_out_and_recovers(proto, count, bs):
     ws.init()
     x2, got, _ = run_ring(case, workspace=ws)
     assert_bit_exact(got, oracle_full(case, x2))
+
+
+# ---------------------------------------------------------------------------
+# many ranks: up to the library's 32, as many channels as still fit one
+# block per SM (N x C <= 152)
+# ---------------------------------------------------------------------------
+def _many_rank_cases():
+    rng = np.random.default_rng(4321)
+    out = []
+    for k, (n, mask) in enumerate([(32, 0b1111), (24, 0b111111), (16, 0x1FF), (9, 0xFFFF), (32, 0x1),
+                                   (17, 0b101)]):
+        for proto in ("Simple", "LL", "LL128"):
+            dtype = "bf16" if (k + len(out)) % 2 else "f32"
+            count = int(rng.integers(1, 400000))
+            ring = rng.permutation(n).tolist()
+            bs = 65536 if proto == "Simple" else 0
+            out.append(gen.RingCase(f"many_n{n}_{proto}_{dtype}_m{mask:x}_c{count}", n, ring, mask, proto, count,
+                                    dtype, "normal", 5000 + len(out), bs, 4))
+    return out
+
+
+@pytest.mark.parametrize("case", _many_rank_cases(), ids=lambda c: c.name)
+def test_many_ranks(case):
+    x, got, _ = run_ring(case)
+    assert_bit_exact(got, oracle_full(case, x))
+
+
+@pytest.mark.parametrize("proto", ["Simple", "LL", "LL128"])
+def test_32_ranks_with_a_ring_per_channel(proto):
+    n, mask, count = 32, 0b1111, 77777
+    rings = [gen.ring_permutation(n, 60 + ch) for ch in range(4)]
+    x = gen.draw("normal", n, count, 61, "f32")
+    _, send = to_device(x, "f32")
+    big_out, recv = guarded_outputs(n, count, "f32")
+    bs = 65536 if proto == "Simple" else 0
+    ws = B.Workspace(n, mask, proto, bs)
+    B.allreduce_ex(send, recv, rings, mask, proto, ws, bs, 4)
+    assert B.get_status(ws) == B.Status.OK
+    check_guards(big_out, count, "f32")
+    want = oracle.ring_allreduce_closed(list(x), rings, mask, OPROTO[proto], bs, 4)
+    assert_bit_exact(device_rows_numpy(recv, "f32"), want)
