@@ -279,6 +279,15 @@ def sweep(torch, B, steps, warmup, peak):
             "busbw_gbs": round(total / t * 7 / 8 / 1e9, 2),
             "us": round(t * 1e6, 1),
             "roofline_frac": round(half_algorithmic_bytes(kind, 8, block, "f32", proto, direct) / t / 1e9 / peak, 3)}
+    # 512 KiB per rank, N=4, ring 0-2-3-1: every protocol on 1, 4 and 12
+    # channels (Simple with a 1 MiB buffer); device time per call from a CUDA
+    # graph of back-to-back calls, and busBW from it
+    s512 = {}
+    for c in gen.sweep_512k_cases():
+        t = graph_latency_ring(c, torch, B) / 1e6
+        s512[c.name] = {"us": round(t * 1e6, 2), "busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
+                        "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
+    out["n4_ring0231_512KiB_f32"] = s512
     # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel. Device
     # latency from a CUDA graph of back-to-back calls (no host enqueue time),
     # and the stream-launch latency as seen between two events.
