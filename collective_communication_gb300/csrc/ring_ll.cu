@@ -863,8 +863,167 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
   }
 }
 
+// ---------------------------------------------------------------------------
+// LL, bulk form: the same roles as LL128's, for LL lines. A tile of
+// kLLTileElems elements starts on a line boundary of both FIFOs; its received
+// lines are bulk-copied into shared memory, every worker thread takes whole
+// units (the elements of one outgoing line, or of one received line on rows
+// that send nothing), accepts each line only by its two flags (a line not yet
+// there is re-polled from global memory), reduces, stores the output and
+// writes the outgoing line with one 16-byte store.
+// ---------------------------------------------------------------------------
+constexpr int kLLTileElems = 3840;
+constexpr int kLLTileLineBytes = kLLTileElems * 4 / 8 * 16;  // binary32 payload: 8 bytes per 16-byte line
+constexpr int kLLBulkMinChunk = 4096;  // chunks at least this long take the bulk form
+
+template <int PROTO>
+__host__ __device__ constexpr int bulk_tile_elems() { return PROTO == kLL ? kLLTileElems : kL8TileElems; }
+template <int PROTO>
+__host__ __device__ constexpr int bulk_line_bytes() { return PROTO == kLL ? kLLTileLineBytes : kL8TileGroups * 512; }
+template <typename T, int PROTO>
+__host__ __device__ constexpr int bulk_stage_bytes() {
+  return bulk_line_bytes<PROTO>() + bulk_tile_elems<PROTO>() * (int)sizeof(T);
+}
+template <typename T, int PROTO>
+__host__ __device__ constexpr int bulk_max_stages() {
+  return kL8SmemBudget / bulk_stage_bytes<T, PROTO>() < kL8MaxStages ? kL8SmemBudget / bulk_stage_bytes<T, PROTO>()
+                                                                     : kL8MaxStages;
+}
+
+// KU input elements of the tile from element e, widened to binary32, zeros
+// past kv: one shared-memory load when all of them are staged.
+template <typename T, int KU>
+__device__ __forceinline__ void ll_input_unit(const char* s_in, const T* g_tile, int e, int kv, int covered,
+                                              float (&x)[4]) {
+  if (kv == KU && e + KU <= covered) {
+    if constexpr (sizeof(T) == 4) {
+      const float2 w = *reinterpret_cast<const float2*>(s_in + e * 4);
+      x[0] = w.x; x[1] = w.y; x[2] = 0.f; x[3] = 0.f;
+    } else if constexpr (KU == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(s_in + e * 2);
+      x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(s_in + e * 2);
+      x[0] = bf16lo(w); x[1] = bf16hi(w); x[2] = 0.f; x[3] = 0.f;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; j++) x[j] = j < kv && j < KU ? l8_input<T>(s_in, g_tile, e + j, covered) : 0.f;
+}
+
+template <typename T, int PRIM>
+__device__ __forceinline__ void ll_bulk_tile(const RingArgs& a, const char* s_lines, const char* s_in,
+                                             const T* g_in_tile, T* g_out_tile, const char* g_rlines, char* g_slines,
+                                             int ne, int covered, uint32_t rflag, uint32_t sflag,
+                                             volatile int* sh_abort, uint64_t info, int ct, int nct) {
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kHasRecv = PRIM != kSend && PRIM != kCopySend;
+  constexpr bool kHasSend = PRIM != kRecv && PRIM != kRecvReduceCopy;
+  constexpr bool kIn = PRIM == kSend || kRecvPartial || PRIM == kCopySend;
+  constexpr bool kFinalOfSum = PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kOut = kFinalOfSum || PRIM == kRecvCopySend || PRIM == kRecv || PRIM == kCopySend;
+  constexpr int EBR = kRecvPartial ? 4 : (int)sizeof(T);                                 // received element bytes
+  constexpr int EBS = (PRIM == kSend || PRIM == kRecvReduceSend) ? 4 : (int)sizeof(T);  // sent element bytes
+  constexpr int KU = 8 / (kHasSend ? EBS : EBR);  // elements of a unit
+  constexpr int LPU = kHasRecv ? KU * EBR / 8 : 0;  // received lines of a unit (2 for bf16's owner row)
+  const int nunits = (ne + KU - 1) / KU;
+  for (int u = ct; u < nunits; u += nct) {
+    const int e = u * KU;
+    const int kv = ne - e < KU ? ne - e : KU;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t fin0 = 0u, fin1 = 0u;  // the unit's final values as raw bits (8 bytes)
+    if (kHasRecv) {
+#pragma unroll
+      for (int l = 0; l < (LPU > 0 ? LPU : 1); l++) {
+        // a unit's second line (bf16's owner row) exists only if it holds elements
+        if (l > 0 && e + l * (8 / EBR) >= ne) break;
+        const int li = u * LPU + l;
+        uint4 rl = *reinterpret_cast<const uint4*>(s_lines + li * 16);
+        if (!ll_ready(rl, rflag)) {
+          rl = ld_line_v4(g_rlines + li * 16);
+          if (!ll_ready(rl, rflag) && !ll_poll(a, g_rlines + li * 16, rflag, rl, sh_abort, info)) return;
+        }
+        if (kRecvPartial) {
+          v[2 * l] = __uint_as_float(rl.x);
+          v[2 * l + 1] = __uint_as_float(rl.z);
+        } else {
+          fin0 = rl.x;
+          fin1 = rl.z;
+        }
+      }
+    }
+    float x[4];
+    if (kIn) ll_input_unit<T, KU>(s_in, g_in_tile, e, kv, covered, x);
+    if (PRIM == kSend) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) v[j] = x[j];
+    } else if (kRecvPartial) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) v[j] = j < kv ? __fadd_rn(v[j], x[j]) : 0.f;
+    }
+    if (kFinalOfSum || PRIM == kCopySend) {
+      const float* f = PRIM == kCopySend ? x : v;  // a bf16 input widened and rounded back is itself
+      if constexpr (sizeof(T) == 4) {
+        fin0 = __float_as_uint(f[0]);
+        fin1 = __float_as_uint(f[1]);
+      } else {
+        fin0 = round_bf16_pair(f[0], f[1]);
+        fin1 = round_bf16_pair(f[2], f[3]);
+      }
+    }
+    if (kOut && kv > 0) store_out_n<T>(g_out_tile + e, kv, KU, make_uint4(fin0, fin1, 0u, 0u));
+    if (kHasSend) {
+      uint4 line;
+      if (EBS == 4 && (PRIM == kSend || PRIM == kRecvReduceSend))
+        line = make_uint4(__float_as_uint(v[0]), sflag, __float_as_uint(v[1]), sflag);
+      else
+        line = make_uint4(fin0, sflag, fin1, sflag);
+      st_line_v4(g_slines + u * 16, line);
+    }
+  }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __grid_constant__ RingArgs a,
+__device__ __forceinline__ void ll_bulk_tile_any(int prim, const RingArgs& a, const char* s_lines, const char* s_in,
+                                                 const T* g_in_tile, T* g_out_tile, const char* g_rlines,
+                                                 char* g_slines, int ne, int covered, uint32_t rflag,
+                                                 uint32_t sflag, volatile int* sh_abort, uint64_t info, int ct,
+                                                 int nct) {
+  switch (prim) {
+    case kSend:
+      ll_bulk_tile<T, kSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag, sflag,
+                             sh_abort, info, ct, nct);
+      break;
+    case kRecvReduceSend:
+      ll_bulk_tile<T, kRecvReduceSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                       rflag, sflag, sh_abort, info, ct, nct);
+      break;
+    case kRecvReduceCopySend:
+      ll_bulk_tile<T, kRecvReduceCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                           rflag, sflag, sh_abort, info, ct, nct);
+      break;
+    case kRecvCopySend:
+      ll_bulk_tile<T, kRecvCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                     rflag, sflag, sh_abort, info, ct, nct);
+      break;
+    case kRecvReduceCopy:
+      ll_bulk_tile<T, kRecvReduceCopy>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered,
+                                       rflag, sflag, sh_abort, info, ct, nct);
+      break;
+    case kCopySend:
+      ll_bulk_tile<T, kCopySend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag,
+                                 sflag, sh_abort, info, ct, nct);
+      break;
+    default:
+      ll_bulk_tile<T, kRecv>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag, sflag,
+                             sh_abort, info, ct, nct);
+      break;
+  }
+}
+
+template <typename T, int PROTO>
+__global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __grid_constant__ RingArgs a,
                                                                         int nstages) {
   extern __shared__ __align__(128) char smem[];
   __shared__ uint64_t bar_ready[kL8Depth], bar_done[kL8Depth], bar_free[kL8Depth];
@@ -873,7 +1032,9 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
   __shared__ int sh_chan;
   __shared__ uint64_t sh_base_send, sh_base_recv;
   constexpr int P = 16 / (int)sizeof(T);
-  constexpr int SB = l8_stage_bytes<T>();
+  constexpr int TE = bulk_tile_elems<PROTO>();
+  constexpr int LB = bulk_line_bytes<PROTO>();
+  constexpr int SB = bulk_stage_bytes<T, PROTO>();
 
   const Geometry& g = a.geo;
   if (threadIdx.x == 0) sh_chan = -1;
@@ -928,14 +1089,22 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
       if (!sh_abort && row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24) | i))
         sh_abort = 1;
       if (!sh_abort && c.nelem > 0 && row_recvs(c.prim)) {
+        // pacing: wait until the step's last line carries its flag
         const int eb = row_recvs_partial(c.prim) ? 4 : (int)sizeof(T);
-        const int64_t ngroups = div_up(c.nelem * eb, 480);
-        const uint64_t* p =
-            reinterpret_cast<const uint64_t*>(fifo_recv + (int64_t)(rstep % kSteps) * step_bytes +
-                                              (4 * (ngroups - 1) + 3) * 128 + 120);
+        const char* slot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
         Spin sp;
-        while (ld_relaxed_u64(p) != rstep + 1) {
-          if (sp.poll(a, info | (9u << 24) | i, rstep + 1)) { sh_abort = 1; break; }
+        if constexpr (PROTO == kLL128) {
+          const int64_t ngroups = div_up(c.nelem * eb, 480);
+          const uint64_t* p = reinterpret_cast<const uint64_t*>(slot + (4 * (ngroups - 1) + 3) * 128 + 120);
+          while (ld_relaxed_u64(p) != rstep + 1) {
+            if (sp.poll(a, info | (9u << 24) | i, rstep + 1)) { sh_abort = 1; break; }
+          }
+        } else {
+          const char* p = slot + (div_up(c.nelem * eb, 8) - 1) * 16;
+          const uint32_t flag = ll_flag(a, rstep);
+          while (!ll_ready(ld_line_v4(p), flag)) {
+            if (sp.poll(a, info | (9u << 24) | i, flag)) { sh_abort = 1; break; }
+          }
         }
       }
       mbar_arrive(&bar_ready[d]);
@@ -963,22 +1132,26 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
       const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       if (has_rcv) fence_proxy_async_global();
-      const int ntiles = (int)div_up(c.nelem, kL8TileElems);
+      const int ntiles = (int)div_up(c.nelem, TE);
       for (int k = 0; k < ntiles; k++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
           sh_abort = 1;
           break;
         }
-        const int64_t e0 = (int64_t)k * kL8TileElems;
-        const int ne = (int)imin(kL8TileElems, c.nelem - e0);
+        const int64_t e0 = (int64_t)k * TE;
+        const int ne = (int)imin(TE, c.nelem - e0);
         const int covered = ne / P * P;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
-        const uint32_t b_rcv = has_rcv ? (uint32_t)div_up((int64_t)ne * eb, 480) * 512u : 0u;
+        // the tile's received lines: whole 4-line groups (LL128) or 16-byte lines (LL)
+        const uint32_t b_rcv = !has_rcv ? 0u
+                               : PROTO == kLL128 ? (uint32_t)div_up((int64_t)ne * eb, 480) * 512u
+                                                 : (uint32_t)div_up((int64_t)ne * eb, 8) * 16u;
+        const int64_t r_off = PROTO == kLL128 ? e0 * eb / 480 * 512 : e0 * eb / 8 * 16;
         char* s_lines = smem + (int64_t)st * SB;
-        char* s_in = s_lines + kL8TileGroups * 512;
+        char* s_in = s_lines + LB;
         mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
-        if (b_rcv) tma_load_1d(s_lines, rslot + e0 * eb / 480 * 512, b_rcv, &bar_full[st], pol);
+        if (b_rcv) tma_load_1d(s_lines, rslot + r_off, b_rcv, &bar_full[st], pol);
         if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         gt++;
       }
@@ -1033,19 +1206,27 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
       char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
-      const int ntiles = (int)div_up(c.nelem, kL8TileElems);
+      const int ntiles = (int)div_up(c.nelem, TE);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (!mbar_wait(a, &bar_full[st], su & 1u, info | (5u << 24) | i)) sh_abort = 1;
-        const int64_t e0 = (int64_t)k * kL8TileElems;
-        const int ne = (int)imin(kL8TileElems, c.nelem - e0);
+        const int64_t e0 = (int64_t)k * TE;
+        const int ne = (int)imin(TE, c.nelem - e0);
         char* s_lines = smem + (int64_t)st * SB;
-        char* s_in = s_lines + kL8TileGroups * 512;
-        // the tile runs on every path so that the workers' barrier counts match
-        l8_tile_any<T>(c.prim, a, s_lines, s_in, in + in_off + e0, out + out_off + e0,
-                       rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne, ne / P * P,
-                       rstep + 1, sstep + 1, &sh_abort, info | (10u << 24) | i, w, &bar_fin, &fin_uses);
+        char* s_in = s_lines + LB;
+        if constexpr (PROTO == kLL128) {
+          // the tile runs on every path so that the workers' barrier counts match
+          l8_tile_any<T>(c.prim, a, s_lines, s_in, in + in_off + e0, out + out_off + e0,
+                         rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne,
+                         ne / P * P, rstep + 1, sstep + 1, &sh_abort, info | (10u << 24) | i, w, &bar_fin,
+                         &fin_uses);
+        } else {
+          ll_bulk_tile_any<T>(c.prim, a, s_lines, s_in, in + in_off + e0, out + out_off + e0,
+                              rslot + e0 * eb_r / 8 * 16, sslot + e0 * eb_s / 8 * 16, sh_abort ? 0 : ne, ne / P * P,
+                              ll_flag(a, rstep), ll_flag(a, sstep), &sh_abort, info | (10u << 24) | i,
+                              threadIdx.x - 96, kL8WorkThreads);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_empty[st]);
         if (sh_abort) {
@@ -1059,6 +1240,27 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_ll128_bulk_kernel(const __
       if (row_sends(c.prim)) sstep++;
     }
   }
+}
+
+template <int PROTO>
+cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int* threads_out) {
+  const int nstages = f32 ? bulk_max_stages<float, PROTO>() : bulk_max_stages<uint16_t, PROTO>();
+  const int smem = nstages * (f32 ? bulk_stage_bytes<float, PROTO>() : bulk_stage_bytes<uint16_t, PROTO>());
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[f32 ? 0 : 1]) {
+    const cudaError_t e =
+        f32 ? cudaFuncSetAttribute(ring_line_bulk_kernel<float, PROTO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   smem)
+            : cudaFuncSetAttribute(ring_line_bulk_kernel<uint16_t, PROTO>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[f32 ? 0 : 1] = true;
+  }
+  cfg.blockDim = dim3(kL8Threads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  if (threads_out) *threads_out = kL8Threads;
+  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<float, PROTO>, a, nstages)
+             : cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<uint16_t, PROTO>, a, nstages);
 }
 
 cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
@@ -1078,6 +1280,15 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   cfg.numAttrs = 1;
   const bool f32 = a.geo.dtype == kF32;
   const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
+  int device = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return e;
+  // LL: the bulk form once a step spans a whole tile (not in the flag-wrap
+  // test mode, whose slot cleanup lives in the polling form)
+  if (a.geo.proto == kLL && first_chunk >= kLLBulkMinChunk && grid <= sms && a.ll_flag_max == 0)
+    return launch_bulk<kLL>(a, cfg, f32, threads_out);
   if (a.geo.proto == kLL) {
     const bool small = div_up(first_chunk, f32 ? LLUnit<float>::kElems : LLUnit<uint16_t>::kElems) <=
                        8 * kThreadsSmall;
@@ -1094,28 +1305,7 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   }
   // LL128: the bulk form once the first loop's chunks span a whole tile,
   // the polling form (lowest latency) for smaller messages.
-  int device = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-  if (e != cudaSuccess) return e;
-  if (first_chunk >= kL8BulkMinChunk && grid <= sms) {
-    const int nstages = f32 ? l8_max_stages<float>() : l8_max_stages<uint16_t>();
-    const int smem = nstages * (f32 ? l8_stage_bytes<float>() : l8_stage_bytes<uint16_t>());
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[f32 ? 0 : 1]) {
-      e = f32 ? cudaFuncSetAttribute(ring_ll128_bulk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-              : cudaFuncSetAttribute(ring_ll128_bulk_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem);
-      if (e != cudaSuccess) return e;
-      attr_set[f32 ? 0 : 1] = true;
-    }
-    cfg.blockDim = dim3(kL8Threads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    if (threads_out) *threads_out = kL8Threads;
-    return f32 ? cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<float>, a, nstages)
-               : cudaLaunchKernelEx(&cfg, ring_ll128_bulk_kernel<uint16_t>, a, nstages);
-  }
+  if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, threads_out);
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;
   return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsSmall>, a)
