@@ -595,10 +595,12 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 // LL128, bulk form: the same lines, flags and head credits, with the loads of
 // large steps moved onto the TMA engine (used when chunks span at least one
 // tile). Roles as in the Simple kernel:
-//   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1) and a
-//                   pacing wait for the step's last line flag; arrives ready[i % D].
-//   warp 1, lane 0  loader: per tile of kL8TileElems elements, bulk copies of
-//                   the tile's received lines and user input into a smem stage.
+//   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1);
+//                   arrives ready[i % D].
+//   warp 1, lane 0  loader: per tile of kL8TileElems elements, a pacing wait for
+//                   the flag of the tile's last received line (LL: of the step's
+//                   last line, once per step), then bulk copies of the tile's
+//                   received lines and user input into a smem stage.
 //   warps 3..18     workers: per 4-line group, check every line's flag in
 //                   shared memory (a line that is not yet there is re-polled
 //                   from global memory until its flag matches), reduce, store
@@ -608,7 +610,7 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 // A line is accepted only by its own flag, exactly as in the polling form.
 // ---------------------------------------------------------------------------
 constexpr int kL8TileElems = 7680;   // 64 groups of binary32 payload, 32 groups of bf16 payload
-constexpr int kL8TileGroups = 64;
+constexpr int kL8TileGroups = kL8TileElems * 4 / 480;
 constexpr int kL8BulkMinChunk = 3840;  // chunks at least this long take the bulk form
 constexpr int kL8Warps = 16;
 constexpr int kL8WorkThreads = 32 * kL8Warps;
@@ -764,6 +766,117 @@ __device__ __forceinline__ void l8_tile_same_layout(const RingArgs& a, const cha
   }
 }
 
+// A lane's piece of a full group (every element present and staged): the
+// input word that holds it, read as one aligned shared-memory vector. A flag
+// lane's piece is half as long and may sit in the upper half of that word.
+template <typename T, int EB>
+__device__ __forceinline__ void l8_full_input(const char* s_in, int el, float (&x)[4]) {
+  if constexpr (sizeof(T) == 4) {
+    const int bo = el * 4;
+    const float4 w4 = *reinterpret_cast<const float4*>(s_in + (bo & ~15));
+    const bool hi = (bo & 8) != 0;
+    x[0] = hi ? w4.z : w4.x;
+    x[1] = hi ? w4.w : w4.y;
+    x[2] = w4.z;
+    x[3] = w4.w;
+  } else {
+    const int bo = el * 2;
+    const uint2 w2 = *reinterpret_cast<const uint2*>(s_in + (bo & ~7));
+    const uint32_t lo = (bo & 4) ? w2.y : w2.x;
+    x[0] = bf16lo(lo);
+    x[1] = bf16hi(lo);
+    x[2] = bf16lo(w2.y);
+    x[3] = bf16hi(w2.y);
+  }
+}
+template <typename T>
+__device__ __forceinline__ uint4 l8_full_raw(const char* s_in, int el) {
+  const int bo = el * (int)sizeof(T);  // payload bytes of the piece = group layout bytes
+  const uint4 w = *reinterpret_cast<const uint4*>(s_in + (bo & ~15));
+  return (bo & 8) ? make_uint4(w.z, w.w, 0u, 0u) : w;
+}
+// Store a lane's output piece: kmax elements of T (16 / EB of them, half as
+// many on flag lanes) from the raw bits in w.
+template <typename T, int EB>
+__device__ __forceinline__ void l8_full_store(T* p, bool flag_lane, uint4 w) {
+  constexpr int kBytes = 16 / EB * (int)sizeof(T);  // 16, or 8 for bf16 from binary32 partial sums
+  if constexpr (kBytes == 16) {
+    if (flag_lane) st_v2(p, make_uint2(w.x, w.y));
+    else st_v4(p, w);
+  } else {
+    if (flag_lane) *reinterpret_cast<uint32_t*>(p) = w.x;
+    else st_v2(p, make_uint2(w.x, w.y));
+  }
+}
+
+// Same values and lines as l8_tile_same_layout for a full tile (kL8TileElems
+// elements, all input staged): every group is whole, so the lanes need no
+// element bounds and each warp's groups are known at compile time.
+template <typename T, int PRIM>
+__device__ __forceinline__ void l8_tile_full(const RingArgs& a, const char* s_lines, const char* s_in,
+                                             T* g_out_tile, const char* g_rlines, char* g_slines, uint64_t rflag,
+                                             uint64_t sflag, volatile int* sh_abort, uint64_t info, int w) {
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kHasRecv = PRIM != kSend && PRIM != kCopySend;
+  constexpr bool kHasSend = PRIM != kRecv && PRIM != kRecvReduceCopy;
+  constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv ||
+                        PRIM == kRecvReduceCopy || PRIM == kCopySend;
+  constexpr int EB = (PRIM == kSend || kRecvPartial) ? 4 : (int)sizeof(T);
+  constexpr int NG = kL8TileElems * EB / 480;
+  static_assert(kL8TileElems * EB % 480 == 0, "a tile is whole groups");
+  constexpr int GPW = (NG + kL8Warps - 1) / kL8Warps;  // groups of a warp: w, w + 16, ...
+  const int gw = NG % kL8Warps == 0 || w < NG % kL8Warps ? GPW : GPW - 1;
+  const LL128Lane L;
+  uint4 rv[GPW];
+  if (kHasRecv) {
+#pragma unroll
+    for (int q = 0; q < GPW; q++)
+      if (q < gw) rv[q] = *reinterpret_cast<const uint4*>(s_lines + (w + q * kL8Warps) * 512 + 16 * L.lane);
+#pragma unroll
+    for (int q = 0; q < GPW; q++)
+      if (q < gw &&
+          !l8_accept(a, rv[q], g_rlines + (w + q * kL8Warps) * 512 + 16 * L.lane, rflag, L.flag_lane, sh_abort, info))
+        return;  // uniform across the warp
+  }
+#pragma unroll
+  for (int q = 0; q < GPW; q++) {
+    if (q >= gw) break;
+    const int gl = w + q * kL8Warps;
+    const int el = (gl * 480 + L.piece_off) / EB;
+    uint4 pay;
+    if constexpr (kRecvPartial || PRIM == kSend) {
+      float x[4];
+      l8_full_input<T, EB>(s_in, el, x);
+      float v[4];
+      if constexpr (kRecvPartial) {
+        v[0] = __fadd_rn(__uint_as_float(rv[q].x), x[0]);
+        v[1] = __fadd_rn(__uint_as_float(rv[q].y), x[1]);
+        v[2] = __fadd_rn(__uint_as_float(rv[q].z), x[2]);
+        v[3] = __fadd_rn(__uint_as_float(rv[q].w), x[3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) v[j] = x[j];
+      }
+      if constexpr (PRIM == kRecvReduceCopy && sizeof(T) == 2)  // bf16 output, rounded once
+        pay = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), 0u, 0u);
+      else
+        pay = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+    } else if constexpr (PRIM == kCopySend) {
+      pay = l8_full_raw<T>(s_in, el);  // already final
+    } else {
+      pay = rv[q];  // final values pass through unchanged
+    }
+    if constexpr (kOut) l8_full_store<T, (PRIM == kRecvReduceCopy ? 4 : (int)sizeof(T))>(g_out_tile + el, L.flag_lane, pay);
+    if constexpr (kHasSend) {
+      if (L.flag_lane) {
+        pay.z = (uint32_t)sflag;
+        pay.w = (uint32_t)(sflag >> 32);
+      }
+      st_line_v4(g_slines + gl * 512 + 16 * L.lane, pay);
+    }
+  }
+}
+
 // bf16 owner row: binary32 partial sums in (120 elements per group), bf16
 // finals out (240 elements per group). The finals are written over the staged
 // bf16 input (each element by the lane that read it), then re-read in the
@@ -826,6 +939,24 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
                                             int ne, int covered, uint64_t rflag, uint64_t sflag,
                                             volatile int* sh_abort, uint64_t info, int w, uint64_t* bar_fin,
                                             uint32_t* fin_uses) {
+  if (ne == kL8TileElems && covered == ne) {
+#define RAR_L8_FULL(P) l8_tile_full<T, P>(a, s_lines, s_in, g_out_tile, g_rlines, g_slines, rflag, sflag, sh_abort, info, w)
+    switch (prim) {
+      case kSend: RAR_L8_FULL(kSend); return;
+      case kRecvReduceSend: RAR_L8_FULL(kRecvReduceSend); return;
+      case kRecvReduceCopySend:
+        if constexpr (sizeof(T) == 4) {
+          RAR_L8_FULL(kRecvReduceCopySend);
+          return;
+        }
+        break;  // bf16's owner row below
+      case kRecvCopySend: RAR_L8_FULL(kRecvCopySend); return;
+      case kRecvReduceCopy: RAR_L8_FULL(kRecvReduceCopy); return;
+      case kCopySend: RAR_L8_FULL(kCopySend); return;
+      default: RAR_L8_FULL(kRecv); return;
+    }
+#undef RAR_L8_FULL
+  }
   switch (prim) {
     case kSend:
       l8_tile_same_layout<T, kSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag,
@@ -1022,6 +1153,55 @@ __device__ __forceinline__ void ll_bulk_tile_any(int prim, const RingArgs& a, co
   }
 }
 
+// Pacing of the bulk form: wait (bounded) until the last of the received
+// lines, `bytes` of them starting at `lines`, carries the flag of step
+// `rstep`. Only a heuristic for when to copy: every line is still
+// accepted by its own flag. False if the wait gave up.
+template <int PROTO>
+__device__ __forceinline__ bool tile_last_line_wait(const RingArgs& a, const char* lines, uint32_t bytes,
+                                                    uint64_t rstep, uint64_t info) {
+  Spin sp;
+  if constexpr (PROTO == kLL128) {
+    const uint64_t* p = reinterpret_cast<const uint64_t*>(lines + bytes - 8);  // flag word of the group's line 3
+    while (ld_relaxed_u64(p) != rstep + 1) {
+      if (sp.poll(a, info, rstep + 1)) return false;
+    }
+  } else {
+    const char* p = lines + bytes - 16;
+    const uint32_t flag = ll_flag(a, rstep);
+    while (!ll_ready(ld_line_v4(p), flag)) {
+      if (sp.poll(a, info, flag)) return false;
+    }
+  }
+  return true;
+}
+
+// LL128 pacing over several tiles at once: the flags of the last lines of
+// tiles k .. k + kPaceBatch - 1 of a step are read together (one round trip);
+// returns the last tile of the prefix that carries the flag, after waiting
+// (bounded) for tile k itself when none does yet, or -1 if the wait gave up.
+constexpr int kPaceBatch = 8;
+__device__ __forceinline__ int l8_tiles_ready(const RingArgs& a, const char* rslot, int k, int ntiles, int64_t nelem,
+                                              int eb, uint64_t rstep, uint64_t info) {
+  uint64_t f[kPaceBatch];
+#pragma unroll
+  for (int j = 0; j < kPaceBatch; j++) {
+    f[j] = 0;
+    if (k + j < ntiles) {
+      // groups up to the end of tile k + j (each tile starts on a group boundary)
+      const int64_t g_end = div_up(imin((int64_t)(k + j + 1) * kL8TileElems, nelem) * eb, 480);
+      f[j] = ld_relaxed_u64(reinterpret_cast<const uint64_t*>(rslot + g_end * 512 - 8));
+    }
+  }
+  int n = 0;
+#pragma unroll
+  for (int j = 0; j < kPaceBatch; j++)
+    if (n == j && k + j < ntiles && f[j] == rstep + 1) n = j + 1;
+  if (n > 0) return k + n - 1;
+  const int64_t g_end = div_up(imin((int64_t)(k + 1) * kL8TileElems, nelem) * eb, 480);
+  return tile_last_line_wait<kLL128>(a, rslot, (uint32_t)(g_end * 512), rstep, info) ? k : -1;
+}
+
 template <typename T, int PROTO>
 __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __grid_constant__ RingArgs a,
                                                                         int nstages) {
@@ -1088,25 +1268,6 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
       if (!sh_abort && row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24) | i))
         sh_abort = 1;
-      if (!sh_abort && c.nelem > 0 && row_recvs(c.prim)) {
-        // pacing: wait until the step's last line carries its flag
-        const int eb = row_recvs_partial(c.prim) ? 4 : (int)sizeof(T);
-        const char* slot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
-        Spin sp;
-        if constexpr (PROTO == kLL128) {
-          const int64_t ngroups = div_up(c.nelem * eb, 480);
-          const uint64_t* p = reinterpret_cast<const uint64_t*>(slot + (4 * (ngroups - 1) + 3) * 128 + 120);
-          while (ld_relaxed_u64(p) != rstep + 1) {
-            if (sp.poll(a, info | (9u << 24) | i, rstep + 1)) { sh_abort = 1; break; }
-          }
-        } else {
-          const char* p = slot + (div_up(c.nelem * eb, 8) - 1) * 16;
-          const uint32_t flag = ll_flag(a, rstep);
-          while (!ll_ready(ld_line_v4(p), flag)) {
-            if (sp.poll(a, info | (9u << 24) | i, flag)) { sh_abort = 1; break; }
-          }
-        }
-      }
       mbar_arrive(&bar_ready[d]);
       if (sh_abort) break;
       if (row_recvs(c.prim)) rstep++;
@@ -1131,8 +1292,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       const bool has_rcv = row_recvs(prim);
       const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
-      if (has_rcv) fence_proxy_async_global();
       const int ntiles = (int)div_up(c.nelem, TE);
+      int ready_upto = -1;  // LL128: the last tile of this step known to carry its flags
       for (int k = 0; k < ntiles; k++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
@@ -1150,6 +1311,28 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
         const int64_t r_off = PROTO == kLL128 ? e0 * eb / 480 * 512 : e0 * eb / 8 * 16;
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + LB;
+        // pacing: LL128 copies a tile's lines once the tile's last line
+        // carries the flag, so that they move while the sender still writes
+        // the step's later tiles (the flags of several tiles are read
+        // together); LL waits once for the step's last line (measured:
+        // per-tile waits made LL slower)
+        if constexpr (PROTO == kLL128) {
+          if (b_rcv && k > ready_upto) {
+            ready_upto = l8_tiles_ready(a, rslot, k, ntiles, c.nelem, eb, rstep, info | (9u << 24) | i);
+            if (ready_upto < 0) {
+              sh_abort = 1;
+              break;
+            }
+            fence_proxy_async_global();
+          }
+        } else if (b_rcv && k == 0) {
+          if (!tile_last_line_wait<PROTO>(a, rslot, (uint32_t)div_up(c.nelem * eb, 8) * 16u, rstep,
+                                          info | (9u << 24) | i)) {
+            sh_abort = 1;
+            break;
+          }
+          fence_proxy_async_global();
+        }
         mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
         if (b_rcv) tma_load_1d(s_lines, rslot + r_off, b_rcv, &bar_full[st], pol);
         if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);

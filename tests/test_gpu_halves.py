@@ -106,6 +106,18 @@ def test_in_place(kind, dtype):
                  direct=(kind == AG and k % 2 == 1))
 
 
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", [RS, AG])
+def test_ll128_whole_tiles(kind, dtype, in_place):
+    """LL128 with its default buffer and blocks of several whole 7680-element
+    tiles (with and without a ragged tail): the bulk form's whole-tile path
+    on the halves' own rows (recvReduceCopy, copySend)."""
+    for k, (n, count, mask) in enumerate([(4, 40000, 0b1), (3, 7680 * 4, 0b10), (6, 7680 * 2 + 16, 0b1001)]):
+        ring = gen.ring_permutation(n, 11 + k)
+        run_half(kind, n, ring, mask, count, dtype, 0, 4, seed=k, in_place=in_place, proto="LL128")
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_allgather_of_reducescatter_is_allreduce_on_the_gpu(dtype):
     """Ring 0..n-1, one channel, one chunk per block: the two halves give the
