@@ -211,6 +211,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Add `bytes` to the current phase's transaction count without arriving:
+// the phase cannot complete before the pending arrival, so copies issued
+// under this count may land before the rest of the phase is set up.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
 // TMA bulk copy global -> shared (no tensor map; 16-byte aligned addresses,
 // size a multiple of 16). Completion is counted on `bar` in bytes. The L2
 // policy marks the source lines evict-first: each is read exactly once.

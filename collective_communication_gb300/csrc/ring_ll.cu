@@ -1311,31 +1311,42 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
         const int64_t r_off = PROTO == kLL128 ? e0 * eb / 480 * 512 : e0 * eb / 8 * 16;
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + LB;
+        // LL128 copies the input (which does not depend on the sender) ahead
+        // of the pacing wait and the lines (measured slower for LL)
+        const bool pace = b_rcv && (PROTO == kLL128 ? k > ready_upto : k == 0);
+        constexpr bool early = PROTO == kLL128;
+        if (early && b_in) {
+          mbar_expect_tx(&bar_full[st], b_in);
+          tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
+        }
         // pacing: LL128 copies a tile's lines once the tile's last line
         // carries the flag, so that they move while the sender still writes
         // the step's later tiles (the flags of several tiles are read
         // together); LL waits once for the step's last line (measured:
         // per-tile waits made LL slower)
+        bool paced = true;
         if constexpr (PROTO == kLL128) {
-          if (b_rcv && k > ready_upto) {
+          if (pace) {
             ready_upto = l8_tiles_ready(a, rslot, k, ntiles, c.nelem, eb, rstep, info | (9u << 24) | i);
-            if (ready_upto < 0) {
-              sh_abort = 1;
-              break;
-            }
-            fence_proxy_async_global();
+            paced = ready_upto >= 0;
+            if (paced) fence_proxy_async_global();
           }
-        } else if (b_rcv && k == 0) {
-          if (!tile_last_line_wait<PROTO>(a, rslot, (uint32_t)div_up(c.nelem * eb, 8) * 16u, rstep,
-                                          info | (9u << 24) | i)) {
-            sh_abort = 1;
-            break;
-          }
-          fence_proxy_async_global();
+        } else if (pace) {
+          paced = tile_last_line_wait<PROTO>(a, rslot, (uint32_t)div_up(c.nelem * eb, 8) * 16u, rstep,
+                                             info | (9u << 24) | i);
+          if (paced) fence_proxy_async_global();
         }
-        mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
+        if (!paced) {
+          if constexpr (early) {
+            mbar_arrive_expect_tx(&bar_full[st], 0u);  // the phase completes once the input landed
+            gt++;
+          }
+          sh_abort = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_full[st], early ? b_rcv : b_in + b_rcv);
         if (b_rcv) tma_load_1d(s_lines, rslot + r_off, b_rcv, &bar_full[st], pol);
-        if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
+        if (!early && b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         gt++;
       }
       if (has_rcv) rstep++;

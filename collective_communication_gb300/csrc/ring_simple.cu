@@ -402,10 +402,6 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
     uint32_t gt = 0;  // tiles issued so far
     for (uint32_t i = 0; c.valid && !sh_abort; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
-      if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) {
-        sh_abort = 1;
-        break;
-      }
       const int prim = c.prim;
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
@@ -418,9 +414,18 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       const bool rcv_bytes = has_rcv && !(rcv_own_out && prim == kRecv);
       const int rcv_eb = recv_is_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
-      if (has_rcv) fence_proxy_async_global();  // the tail acquired above, before bulk reads of the FIFO
       const int ntiles = (int)div_up(c.nelem, kTileElems);
-      for (int k = 0; k < ntiles; k++) {
+      // The slice's first tile copies its input as soon as a stage is free,
+      // before the wait for the slice's tail and credit (the input does not
+      // depend on the peers; copying it early takes its HBM latency off the
+      // chain of handoffs).
+      bool ready = false;
+      for (int k = 0; k < ntiles || !ready; k++) {
+        if (k >= ntiles) {  // an empty slice: only the wait
+          if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) sh_abort = 1;
+          ready = true;
+          break;
+        }
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
           sh_abort = 1;
@@ -433,8 +438,21 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         const uint32_t b_rcv = rcv_bytes ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
         char* s_in = smem + (int64_t)st * SB;
         char* s_rcv = s_in + kTileElems * (int)sizeof(T);
-        mbar_arrive_expect_tx(&bar_full[st], b_in + b_rcv);
-        if (b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
+        if (b_in) {
+          mbar_expect_tx(&bar_full[st], b_in);
+          tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
+        }
+        if (!ready) {
+          ready = true;
+          if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) {
+            mbar_arrive_expect_tx(&bar_full[st], 0u);  // the phase completes once the input landed
+            gt++;
+            sh_abort = 1;
+            break;
+          }
+          if (has_rcv) fence_proxy_async_global();  // the tail acquired by the waiter, before bulk reads of the FIFO
+        }
+        mbar_arrive_expect_tx(&bar_full[st], b_rcv);
         if (b_rcv)
           tma_load_1d(s_rcv, rcv_own_out ? reinterpret_cast<const char*>(out + out_off + e0) : rslot + e0 * rcv_eb,
                       b_rcv, &bar_full[st], pol);
