@@ -85,7 +85,7 @@ struct StPack<uint16_t> {
   }
 };
 
-// Thread 0's bounded wait until *p >= want. Returns false when it gave up.
+// One thread's bounded wait until *p >= want. Returns false when it gave up.
 __device__ __forceinline__ bool os_wait_at_least(const StagedArgs& a, const uint64_t* p, uint64_t want,
                                                  uint64_t info) {
   Spin sp;
@@ -121,18 +121,21 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
       atomicCAS(&h->status, 0u, kErrAbort);
       sh_stop = 1;
     } else {
-      const uint64_t s = ld_acquire_u64(&me->tx_seq);
-      sh_s = s;
-      for (int q = 0; q < N && !sh_stop; q++)
-        if (s + 1 > kStagingSlots &&
-            !os_wait_at_least(a, &os_control(a, q)->ack_seq, s + 1 - kStagingSlots, info | (1u << 24) | q))
-          sh_stop = 1;
+      sh_s = ld_acquire_u64(&me->tx_seq);
     }
   }
   __syncthreads();
   if (sh_stop) return;
   const uint64_t s = sh_s;
   const int64_t sb = sh_slot_bytes;
+  // guard: thread q < N waits for rank q's acknowledgement (the N waits run
+  // side by side; the block barrier then orders the copy after all of them)
+  if (threadIdx.x < N && s + 1 > kStagingSlots &&
+      !os_wait_at_least(a, &os_control(a, threadIdx.x)->ack_seq, s + 1 - kStagingSlots,
+                        info | (1u << 24) | threadIdx.x))
+    sh_stop = 1;
+  __syncthreads();
+  if (sh_stop) return;
 
   // ---- copy the rank's input into its slot ----
   const int64_t npack = a.count / P;
@@ -152,9 +155,10 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
     fence_acq_rel_gpu();  // the block's copies are visible before its count
     const uint64_t old = atom_add_acq_rel_u64(&me->done, 1);
     if (old % (uint64_t)G == (uint64_t)G - 1) st_release_u64(&me->tx_seq, s + 1);
-    for (int q = 0; q < N && !sh_stop; q++)
-      if (!os_wait_at_least(a, &os_control(a, q)->tx_seq, s + 1, info | (2u << 24) | q)) sh_stop = 1;
   }
+  // thread q < N waits for rank q's sequence number, side by side
+  if (threadIdx.x < N && !os_wait_at_least(a, &os_control(a, threadIdx.x)->tx_seq, s + 1, info | (2u << 24) | threadIdx.x))
+    sh_stop = 1;
   __syncthreads();
   if (sh_stop) return;
 
