@@ -24,9 +24,11 @@
 //            publishes tx_seq[r] = s + 1 (release).
 //   wait     every block waits until tx_seq[q] >= s + 1 for all q (acquire).
 //   reduce   out_r = T(sum over q = 0..N-1 of slot (q, s % RING)), binary32, in
-//            user-rank order, rounded once for bf16.
-//   ack      fence, atomicAdd(read[r], 1); the last block publishes
-//            ack_seq[r] = s + 1: rank r has finished reading call s's slots.
+//            user-rank order, rounded once for bf16; rank r's blocks take
+//            chunks of packs from a counter grab[r][s % RING].
+//   ack      fence, atomicAdd(read[r], 1); the last block resets grab[r][s %
+//            RING] and publishes ack_seq[r] = s + 1: rank r has finished
+//            reading call s's slots.
 // A block reads tx_seq before its own atomicAdd, and the block that publishes
 // s + 1 exists only after every block of the launch has added, so no block of
 // this launch can read s + 1 at entry. All N*G blocks wait on each other, so
@@ -38,6 +40,7 @@
 namespace rar {
 
 constexpr int kStagedThreads = 256;
+constexpr int64_t kGrabPacks = 2 * kStagedThreads;  // packs of one reduce chunk
 
 __device__ __forceinline__ OsHeader* os_header(const StagedArgs& a) { return (OsHeader*)a.ws; }
 __device__ __forceinline__ OsControl* os_control(const StagedArgs& a, int rank) {
@@ -102,6 +105,7 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   __shared__ uint64_t sh_s;
   __shared__ int64_t sh_slot_bytes;
   __shared__ int sh_stop;
+  __shared__ int64_t sh_chunk[2];
   const int N = a.nranks, G = a.blocks_per_rank;
   const int rank = blockIdx.x % N;
   const int j = blockIdx.x / N;
@@ -155,6 +159,7 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
     fence_acq_rel_gpu();  // the block's copies are visible before its count
     const uint64_t old = atom_add_acq_rel_u64(&me->done, 1);
     if (old % (uint64_t)G == (uint64_t)G - 1) st_release_u64(&me->tx_seq, s + 1);
+    sh_chunk[0] = (int64_t)atomicAdd(reinterpret_cast<unsigned long long*>(&me->grab[s % kStagingSlots]), 1ull);
   }
   // thread q < N waits for rank q's sequence number, side by side
   if (threadIdx.x < N && !os_wait_at_least(a, &os_control(a, threadIdx.x)->tx_seq, s + 1, info | (2u << 24) | threadIdx.x))
@@ -163,8 +168,20 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   if (sh_stop) return;
 
   // ---- reduce the N staged copies, in user-rank order ----
+  // The rank's packs go out in chunks of kGrabPacks from a counter of the
+  // slot, so that blocks on SMs with more L2 bandwidth take more chunks (the
+  // first chunk was taken before the wait). The call's last reader resets the
+  // counter before it acknowledges; the slot's next call passes the guard
+  // only after that.
   T* out = reinterpret_cast<T*>(a.recv[rank]);
-  for (int64_t p = (int64_t)j * kStagedThreads + threadIdx.x; p < npack; p += (int64_t)G * kStagedThreads) {
+  const int64_t nchunks = (npack + kGrabPacks - 1) / kGrabPacks;
+  unsigned long long* grab = reinterpret_cast<unsigned long long*>(&me->grab[s % kStagingSlots]);
+  for (int cur = 0;; cur ^= 1) {
+    const int64_t chunk = sh_chunk[cur];
+    if (chunk >= nchunks) break;
+    if (threadIdx.x == 0) sh_chunk[cur ^ 1] = (int64_t)atomicAdd(grab, 1ull);  // the next chunk, ahead
+    const int64_t p_end = (chunk + 1) * kGrabPacks < npack ? (chunk + 1) * kGrabPacks : npack;
+    for (int64_t p = chunk * kGrabPacks + threadIdx.x; p < p_end; p += kStagedThreads) {
     float acc[8];
     for (int q0 = 0; q0 < N; q0 += kBatchRanks) {
       uint4 w[kBatchRanks];
@@ -187,6 +204,8 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
       }
     }
     st_v4(out + p * P, StPack<T>::narrow(acc));
+    }
+    __syncthreads();  // every thread has read sh_chunk[cur]; thread 0's next chunk is visible
   }
   if (j == 0) {
     for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kStagedThreads) {
@@ -201,7 +220,10 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   if (threadIdx.x == 0) {
     fence_acq_rel_gpu();
     const uint64_t old = atom_add_acq_rel_u64(&me->read, 1);
-    if (old % (uint64_t)G == (uint64_t)G - 1 && a.fault != kFaultDropAck) st_release_u64(&me->ack_seq, s + 1);
+    if (old % (uint64_t)G == (uint64_t)G - 1) {
+      st_relaxed_u64(&me->grab[s % kStagingSlots], 0);  // every block of this call has taken its last chunk
+      if (a.fault != kFaultDropAck) st_release_u64(&me->ack_seq, s + 1);
+    }
   }
 }
 

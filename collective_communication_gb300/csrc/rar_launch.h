@@ -24,7 +24,7 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream);
 // ---- staged one-shot (oneshot_staged.cu) ----
 // Workspace: a 4 KiB header, one OsControl per rank (rounded up to 4 KiB),
 // then kStagingSlots slots of slot_bytes per rank.
-constexpr uint32_t kStagedMagic = 0x31534152u;  // "RAS1"
+constexpr uint32_t kStagedMagic = 0x32534152u;  // "RAS2"
 constexpr int kStagingSlots = 4;                // slots per rank, reused round-robin
 constexpr int kStagedBlocksPerSm = 4;           // grid = nranks * (SMs * 4 / nranks) blocks
 
@@ -53,6 +53,8 @@ struct OsControl {
   uint64_t pad2[15];
   uint64_t read;  // blocks that finished reducing, over all calls
   uint64_t pad3[15];
+  uint64_t grab[kStagingSlots];  // reduce chunks handed out in the call using each slot (reset after it)
+  uint64_t pad4[16 - kStagingSlots];
 };
 
 struct StagedArgs {

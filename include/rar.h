@@ -246,7 +246,7 @@ RAR_API rar_status rar_oneshot(const void* const* sendbufs, void* const* recvbuf
  *
  * rar_oneshot_workspace_bytes: bytes of a workspace for calls of up to
  *   max_count elements of dtype over nranks ranks (0 for invalid arguments):
- *   a 4 KiB header, 512 B of counters per rank, 4 slots per rank.
+ *   a 4 KiB header, 640 B of counters per rank, 4 slots per rank.
  * rar_oneshot_workspace_init: zero the header and counters, record the
  *   configuration (nranks, dtype, max_count, and the grid, 4 * SMs / nranks
  *   blocks per rank on the current device); enqueued on `stream`. Errors:

@@ -227,7 +227,7 @@ def test_staged_oneshot_workspace_bytes_formula(lib):
     for n in (1, 2, 8, 32):
         for count, dt, eb in ((1, 0, 4), (7168 * 512, 1, 2), (1000, 1, 2), (4097, 0, 4)):
             slot = -(-count * eb // 256) * 256
-            want = 4096 + -(-n * 512 // 4096) * 4096 + n * 4 * slot
+            want = 4096 + -(-n * 640 // 4096) * 4096 + n * 4 * slot
             assert L.rar_oneshot_workspace_bytes(n, count, dt) == want
     assert L.rar_oneshot_workspace_bytes(0, 10, 0) == 0
     assert L.rar_oneshot_workspace_bytes(33, 10, 0) == 0
