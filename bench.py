@@ -287,6 +287,18 @@ def sweep(torch, B, steps, warmup, peak):
         t = graph_latency_ring(c, torch, B) / 1e6
         s512[c.name] = {"us": round(t * 1e6, 2), "busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
                         "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
+    # the same workload on 12 channels with a ring per channel: the six N=4
+    # rings through rank 0 listed for channels 0-5 and repeated on 6-11 in
+    # the channel-parallel page's 12-channel graph
+    six = [[0, 1, 2, 3], [0, 1, 3, 2], [0, 2, 3, 1], [0, 2, 1, 3], [0, 3, 1, 2], [0, 3, 2, 1]]
+    for c in gen.sweep_512k_cases():
+        if c.mask != 0xFFF:
+            continue
+        c.ring = six + six
+        c.name = c.name.replace("_ch12_", "_ch12_page_rings_")
+        t = graph_latency_ring(c, torch, B) / 1e6
+        s512[c.name] = {"us": round(t * 1e6, 2), "busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2),
+                        "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
     out["n4_ring0231_512KiB_f32"] = s512
     # small messages: 4 KiB per rank, N=4, ring 0-2-3-1, one channel. Device
     # latency from a CUDA graph of back-to-back calls (no host enqueue time),
@@ -398,8 +410,8 @@ def graph_latency_ring(case, torch, B):
     send = [x[r] for r in range(case.nranks)]
     recv = [y[r] for r in range(case.nranks)]
     ws = B.Workspace(case.nranks, case.mask, case.proto, case.buff_size)
-    lat = graph_latency(lambda: B.allreduce(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size,
-                                            case.chunk_steps), torch)
+    lat = graph_latency(lambda: B.allreduce_ex(send, recv, case.ring, case.mask, case.proto, ws, case.buff_size,
+                                               case.chunk_steps), torch)
     if B.get_status(ws) != B.Status.OK:
         raise RuntimeError("graph replay: device status not OK")
     return lat
