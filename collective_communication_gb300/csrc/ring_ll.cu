@@ -1115,12 +1115,117 @@ __device__ __forceinline__ void ll_bulk_tile(const RingArgs& a, const char* s_li
   }
 }
 
+// Same values and lines as ll_bulk_tile for a whole tile (kLLTileElems
+// elements, all input staged): every unit is full, so the threads need no
+// element bounds and each thread's units are known at compile time.
+template <typename T, int PRIM>
+__device__ __forceinline__ void ll_bulk_tile_full(const RingArgs& a, const char* s_lines, const char* s_in,
+                                                  T* g_out_tile, const char* g_rlines, char* g_slines, uint32_t rflag,
+                                                  uint32_t sflag, volatile int* sh_abort, uint64_t info, int ct) {
+  constexpr bool kRecvPartial = PRIM == kRecvReduceSend || PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kHasRecv = PRIM != kSend && PRIM != kCopySend;
+  constexpr bool kHasSend = PRIM != kRecv && PRIM != kRecvReduceCopy;
+  constexpr bool kIn = PRIM == kSend || kRecvPartial || PRIM == kCopySend;
+  constexpr bool kFinalOfSum = PRIM == kRecvReduceCopySend || PRIM == kRecvReduceCopy;
+  constexpr bool kOut = kFinalOfSum || PRIM == kRecvCopySend || PRIM == kRecv || PRIM == kCopySend;
+  constexpr int EBR = kRecvPartial ? 4 : (int)sizeof(T);
+  constexpr int EBS = (PRIM == kSend || PRIM == kRecvReduceSend) ? 4 : (int)sizeof(T);
+  constexpr int KU = 8 / (kHasSend ? EBS : EBR);
+  constexpr int LPU = kHasRecv ? KU * EBR / 8 : 0;
+  constexpr int NU = kLLTileElems / KU;  // units of a whole tile
+  constexpr int RPT = (NU + kL8WorkThreads - 1) / kL8WorkThreads;
+  static_assert(kLLTileElems % KU == 0, "whole units");
+#pragma unroll
+  for (int r = 0; r < RPT; r++) {
+    const int u = ct + r * kL8WorkThreads;
+    if (NU % kL8WorkThreads != 0 && u >= NU) break;
+    const int e = u * KU;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t fin0 = 0u, fin1 = 0u;
+    if constexpr (kHasRecv) {
+#pragma unroll
+      for (int l = 0; l < LPU; l++) {
+        const int li = u * LPU + l;
+        uint4 rl = *reinterpret_cast<const uint4*>(s_lines + li * 16);
+        if (!ll_ready(rl, rflag)) {
+          rl = ld_line_v4(g_rlines + li * 16);
+          if (!ll_ready(rl, rflag) && !ll_poll(a, g_rlines + li * 16, rflag, rl, sh_abort, info)) return;
+        }
+        if constexpr (kRecvPartial) {
+          v[2 * l] = __uint_as_float(rl.x);
+          v[2 * l + 1] = __uint_as_float(rl.z);
+        } else {
+          fin0 = rl.x;
+          fin1 = rl.z;
+        }
+      }
+    }
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (kIn) {
+      if constexpr (sizeof(T) == 4) {
+        const float2 w = *reinterpret_cast<const float2*>(s_in + e * 4);
+        x[0] = w.x;
+        x[1] = w.y;
+      } else if constexpr (KU == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(s_in + e * 2);
+        x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+      } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(s_in + e * 2);
+        x[0] = bf16lo(w);
+        x[1] = bf16hi(w);
+      }
+    }
+    if constexpr (PRIM == kSend) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) v[j] = x[j];
+    } else if constexpr (kRecvPartial) {
+#pragma unroll
+      for (int j = 0; j < KU; j++) v[j] = __fadd_rn(v[j], x[j]);
+    }
+    if constexpr (kFinalOfSum || PRIM == kCopySend) {
+      const float* f = PRIM == kCopySend ? x : v;
+      if constexpr (sizeof(T) == 4) {
+        fin0 = __float_as_uint(f[0]);
+        fin1 = __float_as_uint(f[1]);
+      } else {
+        fin0 = round_bf16_pair(f[0], f[1]);
+        fin1 = round_bf16_pair(f[2], f[3]);
+      }
+    }
+    if constexpr (kOut) {
+      if constexpr (KU * sizeof(T) == 8) st_v2(g_out_tile + e, make_uint2(fin0, fin1));
+      else *reinterpret_cast<uint32_t*>(g_out_tile + e) = fin0;
+    }
+    if constexpr (kHasSend) {
+      uint4 line;
+      if constexpr (EBS == 4 && (PRIM == kSend || PRIM == kRecvReduceSend))
+        line = make_uint4(__float_as_uint(v[0]), sflag, __float_as_uint(v[1]), sflag);
+      else
+        line = make_uint4(fin0, sflag, fin1, sflag);
+      st_line_v4(g_slines + u * 16, line);
+    }
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void ll_bulk_tile_any(int prim, const RingArgs& a, const char* s_lines, const char* s_in,
                                                  const T* g_in_tile, T* g_out_tile, const char* g_rlines,
                                                  char* g_slines, int ne, int covered, uint32_t rflag,
                                                  uint32_t sflag, volatile int* sh_abort, uint64_t info, int ct,
                                                  int nct) {
+  if (ne == kLLTileElems && covered == ne && nct == kL8WorkThreads) {
+#define RAR_LL_FULL(P) ll_bulk_tile_full<T, P>(a, s_lines, s_in, g_out_tile, g_rlines, g_slines, rflag, sflag, sh_abort, info, ct)
+    switch (prim) {
+      case kSend: RAR_LL_FULL(kSend); return;
+      case kRecvReduceSend: RAR_LL_FULL(kRecvReduceSend); return;
+      case kRecvReduceCopySend: RAR_LL_FULL(kRecvReduceCopySend); return;
+      case kRecvCopySend: RAR_LL_FULL(kRecvCopySend); return;
+      case kRecvReduceCopy: RAR_LL_FULL(kRecvReduceCopy); return;
+      case kCopySend: RAR_LL_FULL(kCopySend); return;
+      default: RAR_LL_FULL(kRecv); return;
+    }
+#undef RAR_LL_FULL
+  }
   switch (prim) {
     case kSend:
       ll_bulk_tile<T, kSend>(a, s_lines, s_in, g_in_tile, g_out_tile, g_rlines, g_slines, ne, covered, rflag, sflag,
