@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 // ---------------------------------------------------------------------------
 constexpr int kL8TileElems = 7680;   // 64 groups of binary32 payload, 32 groups of bf16 payload
 constexpr int kL8TileGroups = kL8TileElems * 4 / 480;
-constexpr int kL8BulkMinChunk = 3840;  // chunks at least this long take the bulk form
+constexpr int kL8BulkMinChunk = 960;  // chunks at least this long take the bulk form (measured: 480-7680)
 constexpr int kL8Warps = 16;
 constexpr int kL8WorkThreads = 32 * kL8Warps;
 constexpr int kL8Threads = 32 * 3 + kL8WorkThreads;
@@ -1005,7 +1005,7 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
 // ---------------------------------------------------------------------------
 constexpr int kLLTileElems = 3840;
 constexpr int kLLTileLineBytes = kLLTileElems * 4 / 8 * 16;  // binary32 payload: 8 bytes per 16-byte line
-constexpr int kLLBulkMinChunk = 4096;  // chunks at least this long take the bulk form
+constexpr int kLLBulkMinChunk = 1024;  // chunks at least this long take the bulk form (measured: 1-8192)
 
 template <int PROTO>
 __host__ __device__ constexpr int bulk_tile_elems() { return PROTO == kLL ? kLLTileElems : kL8TileElems; }
@@ -1584,8 +1584,9 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return e;
-  // LL: the bulk form once a step spans a whole tile (not in the flag-wrap
-  // test mode, whose slot cleanup lives in the polling form)
+  // LL: the bulk form from 1024-element chunks (not in the flag-wrap test
+  // mode, whose slot cleanup lives in the polling form); below that the
+  // polling form has the lower latency
   if (a.geo.proto == kLL && first_chunk >= kLLBulkMinChunk && grid <= sms && a.ll_flag_max == 0)
     return launch_bulk<kLL>(a, cfg, f32, threads_out);
   if (a.geo.proto == kLL) {
@@ -1602,8 +1603,8 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
     return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLarge>, a)
                : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLarge>, a);
   }
-  // LL128: the bulk form once the first loop's chunks span a whole tile,
-  // the polling form (lowest latency) for smaller messages.
+  // LL128: the bulk form from 960-element chunks, the polling form (lowest
+  // latency) for smaller messages.
   if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, threads_out);
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;

@@ -232,8 +232,8 @@ def test_sparse_mask_size_sweep(case):
 
 
 # ---------------------------------------------------------------------------
-# LL128: the bulk (TMA-staged) form for chunks of at least one 3840-element
-# tile, the polling form below that; both must give the oracle's bytes
+# LL128: the bulk (TMA-staged) form for first-loop chunks of at least 960
+# elements, the polling form below that; both must give the oracle's bytes
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("in_place", [False, True])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -252,6 +252,22 @@ def test_ll128_forms_alternate_on_one_workspace():
     for k, count in enumerate([1000, 200003, 777, 150000, 3, 300001]):
         dtype = "bf16" if k % 2 else "f32"
         case = gen.RingCase("alt", 4, gen.RING_0231, 0b11, "LL128", count, dtype, "normal", 70 + k, 0, 4)
+        x, got, _ = run_ring(case, workspace=ws)
+        assert_bit_exact(got, oracle_full(case, x))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("proto,thr", [("LL", 1024), ("LL128", 960)])
+def test_line_forms_at_the_bulk_threshold(proto, thr, dtype):
+    """First-loop chunks just below, at and above the bulk form's threshold
+    (LL 1024, LL128 960 elements) on one workspace, so that the two forms
+    alternate; odd calls end in a ragged chunk."""
+    n = 3
+    e = 4 if dtype == "f32" else 8
+    ws = B.Workspace(n, 0b1, proto, 0)
+    for k, chunk in enumerate([thr - e, thr, thr + e, thr - e, 4 * thr]):
+        count = n * chunk - (k % 2)
+        case = gen.RingCase("thr", n, [0, 2, 1], 0b1, proto, count, dtype, "normal", 80 + k, 0, 4)
         x, got, _ = run_ring(case, workspace=ws)
         assert_bit_exact(got, oracle_full(case, x))
 
