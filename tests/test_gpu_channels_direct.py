@@ -101,3 +101,26 @@ def test_direct_64MiB_sampled():
     want, _ = oracle.ring_closed_at(xs, rings, mask, oracle.SIMPLE, idx, count, bs, 4)
     got = y[0].index_select(0, it).cpu().numpy()
     assert got.tobytes() == want.tobytes()
+
+
+def _random_default_buffer_case(seed):
+    rng = np.random.default_rng(4000 + seed)
+    n = int(rng.integers(2, 13))
+    proto = ["LL", "LL128", "Simple"][seed % 3]
+    dtype = "bf16" if seed % 2 else "f32"
+    mask = int(rng.integers(1, 1 << 12))
+    while n * bin(mask).count("1") > 152:  # one block per SM
+        mask &= mask - 1
+    nch = bin(mask).count("1")
+    rings = [rng.permutation(n).tolist() for _ in range(nch)] if seed % 4 >= 2 else rng.permutation(n).tolist()
+    count = int(rng.integers(1, 1 << int(rng.integers(1, 22))))
+    return n, rings, mask, proto, count, dtype, bool(rng.integers(0, 2))
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_default_buffers(seed):
+    """The protocols' default buffers (the forms and tile paths the bench
+    uses) over random rank counts up to 12, masks over 12 channels, one ring
+    or one per channel, sizes from 1 element to 2 Mi, in place or not."""
+    n, rings, mask, proto, count, dtype, in_place = _random_default_buffer_case(seed)
+    run_ex(n, rings, mask, proto, count, dtype, 0, 4, seed=seed, in_place=in_place)
