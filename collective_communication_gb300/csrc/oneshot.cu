@@ -16,6 +16,8 @@
 //
 // Sum: binary32, in user-rank order 0..N-1, starting from x_0 (no added
 // zero), rounded once to bf16 for bf16 data.
+#include <cstdio>
+
 #include "rar_launch.h"
 
 namespace rar {
@@ -156,6 +158,10 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
   if (tiles < 1) tiles = 1;
   cfg.gridDim = dim3((unsigned)(tiles * a.nranks));
   cfg.blockDim = dim3(kOneShotThreads);
+  if (trace_on())
+    std::fprintf(stderr, "rar trace: oneshot nranks=%d count=%lld dtype=%s grid=%u (block b: rank b %% %d, tile b / %d) "
+                 "threads=%d kernel=oneshot_kernel\n", a.nranks, (long long)a.count, a.dtype == kF32 ? "f32" : "bf16",
+                 cfg.gridDim.x, a.nranks, a.nranks, kOneShotThreads);
   if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_kernel<float>, a);
   return cudaLaunchKernelEx(&cfg, oneshot_kernel<uint16_t>, a);
 }

@@ -35,6 +35,8 @@
 // the launch is cooperative (all blocks resident, or the launch is refused).
 // Every wait is bounded; a wait that runs out raises the workspace's abort
 // flag and every other wait then ends too.
+#include <cstdio>
+
 #include "rar_launch.h"
 
 namespace rar {
@@ -242,6 +244,10 @@ cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (trace_on())
+    std::fprintf(stderr, "rar trace: oneshot_staged nranks=%d count=%lld dtype=%s grid=%u blocks_per_rank=%d "
+                 "threads=%d kernel=oneshot_staged_kernel (cooperative)\n", a.nranks, (long long)a.count,
+                 a.dtype == kF32 ? "f32" : "bf16", cfg.gridDim.x, a.blocks_per_rank, kStagedThreads);
   if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_staged_kernel<float>, a);
   return cudaLaunchKernelEx(&cfg, oneshot_staged_kernel<uint16_t>, a);
 }

@@ -8,6 +8,7 @@
 //   [OS89] "perf(osar): all-reduce 5커널 → 3커널 (가드·웨이트 프롤로그 융합) - #89"
 //          (review finding: an empty input must not advance any state)
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -23,6 +24,18 @@ std::atomic<uint32_t> g_ll_flag_max{0};
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
+}  // namespace
+
+bool trace_on() {
+  static const bool on = [] {
+    const char* env = std::getenv("RAR_TRACE");
+    return env != nullptr && env[0] != '\0' && std::strcmp(env, "0") != 0;
+  }();
+  return on;
+}
+
+namespace {
+
 uint64_t spin_timeout_ns() {
   uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
   if (t != 0) return t;
@@ -35,6 +48,35 @@ uint64_t spin_timeout_ns() {
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+const char* kind_name(int kind) {
+  return kind == kReduceScatter ? "reduce_scatter" : kind == kAllGather ? "all_gather" : "allreduce";
+}
+const char* proto_name(int proto) { return proto == kLL ? "LL" : proto == kLL128 ? "LL128" : "Simple"; }
+
+// One call's resolved geometry ([C23] "Kernel 如何把 Block 映射到 Channel";
+// [C12] "runRing 的数据切分"): grid, block -> channel, per-channel range and
+// loops, chunk and slice sizes.
+void trace_geometry(int kind, const Geometry& g, uint64_t mask, int nrings, bool direct) {
+  std::fprintf(stderr,
+               "rar trace: %s nranks=%d count=%lld dtype=%s proto=%s mask=0x%llx grid=%d buff=%lld "
+               "step_bytes=%lld chunk_elems=%lld steps_per_slice=%d slices_per_chunk=%d per_channel=%lld "
+               "rings=%d direct=%d\n",
+               kind_name(kind), g.nranks, (long long)g.count, g.dtype == kF32 ? "f32" : "bf16", proto_name(g.proto),
+               (unsigned long long)mask, g.nranks * g.nchan, (long long)g.buff_size, (long long)g.step_bytes,
+               (long long)g.chunk_elems, g.sps, g.spc, (long long)g.per_channel, nrings, direct ? 1 : 0);
+  int n = 0;
+  for (int b = 0; b < kMaxChannels; b++) {
+    if (((mask >> b) & 1ull) == 0) continue;
+    int64_t go, cc;
+    channel_range(g, n, &go, &cc);
+    std::fprintf(stderr,
+                 "rar trace:   channel %d id %d blocks %d+%d*rank offset %lld count %lld loops %lld first_chunk %lld\n",
+                 n, b, n, g.nchan, (long long)go, (long long)cc, (long long)div_up(cc, loop_count(g)),
+                 (long long)(cc > 0 ? loop_chunk_count(g, cc) : 0));
+    n++;
+  }
+}
 
 // Ring setup ([C12] "ring index 如何计算"): check that following `next` from
 // rank 0 visits every rank once and comes back ("ring does not loop back"),
@@ -211,6 +253,7 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
   rar_status st = kind == kAllReduce ? check_buffers(sendbufs, recvbufs, nranks, block, true)
                                      : check_half_buffers(kind, sendbufs, recvbufs, nranks, block);
   if (st != RAR_OK) return st;
+  if (trace_on()) trace_geometry(kind, g, channelMask, nrings, direct);
   if (workspace == nullptr) return RAR_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
   if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, g.nchan, g.buff_size)) return RAR_ERR_WORKSPACE;

@@ -78,6 +78,10 @@ inline int64_t staged_workspace_bytes(int nranks, int64_t max_count, int elem_by
   return staged_stage_offset(nranks) + (int64_t)nranks * kStagingSlots * staged_slot_bytes(max_count, elem_bytes);
 }
 int staged_blocks_per_rank(int nranks, int sms);
+
+// Host-side tracing: RAR_TRACE set to anything but "0" in the environment
+// makes every call print its resolved geometry and kernel to stderr.
+bool trace_on();
 cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream);
 
 }  // namespace rar

@@ -26,7 +26,9 @@
 // bytes of group g map to the lanes so that every user access stays aligned:
 // lanes with l%8 < 7 carry group bytes 16*(7*(l/8) + l%8) .. +16, the four
 // flag lanes carry bytes 448 + 8*(l/8) .. +8.
-#include "rar_device.cuh"
+#include <cstdio>
+
+#include "rar_launch.h"
 
 namespace rar {
 
@@ -1558,8 +1560,17 @@ cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int
   cfg.blockDim = dim3(kL8Threads);
   cfg.dynamicSmemBytes = (size_t)smem;
   if (threads_out) *threads_out = kL8Threads;
+  if (trace_on())
+    std::fprintf(stderr, "rar trace:   kernel ring_line_bulk_kernel<%s, %s> grid %u threads %d stages %d smem %d\n",
+                 f32 ? "float" : "bf16", PROTO == kLL ? "LL" : "LL128", cfg.gridDim.x, kL8Threads, nstages, smem);
   return f32 ? cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<float, PROTO>, a, nstages)
              : cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<uint16_t, PROTO>, a, nstages);
+}
+
+void trace_polling(const char* proto, bool f32, int grid, int threads) {
+  if (trace_on())
+    std::fprintf(stderr, "rar trace:   kernel ring_line_kernel<%s, %s, %d> grid %d threads %d\n", f32 ? "float" : "bf16",
+                 proto, threads, grid, threads);
 }
 
 cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
@@ -1595,11 +1606,13 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
     if (small) {
       cfg.blockDim = dim3(kThreadsSmall);
       if (threads_out) *threads_out = kThreadsSmall;
+      trace_polling("LL", f32, grid, kThreadsSmall);
       return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsSmall>, a)
                  : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsSmall>, a);
     }
     cfg.blockDim = dim3(kThreadsLarge);
     if (threads_out) *threads_out = kThreadsLarge;
+    trace_polling("LL", f32, grid, kThreadsLarge);
     return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLarge>, a)
                : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLarge>, a);
   }
@@ -1608,6 +1621,7 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, threads_out);
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;
+  trace_polling("LL128", f32, grid, kThreadsSmall);
   return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsSmall>, a)
              : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL128, kThreadsSmall>, a);
 }

@@ -28,7 +28,9 @@
 // `nstages` tiles between loader and workers (about 190 KB of loads in flight
 // per SM). Empty slices still wait and post, so both ends of every connection
 // count the same steps.
-#include "rar_device.cuh"
+#include <cstdio>
+
+#include "rar_launch.h"
 
 namespace rar {
 
@@ -581,6 +583,9 @@ cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (threads_out) *threads_out = kSimpleThreads;
+  if (trace_on())
+    std::fprintf(stderr, "rar trace:   kernel ring_simple_kernel<%s> grid %d threads %d stages %d smem %d\n",
+                 f32 ? "float" : "bf16", grid, kSimpleThreads, nstages, smem);
   if (f32) return cudaLaunchKernelEx(&cfg, ring_simple_kernel<float>, a, nstages);
   return cudaLaunchKernelEx(&cfg, ring_simple_kernel<uint16_t>, a, nstages);
 }

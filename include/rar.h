@@ -27,6 +27,12 @@
  *    word in the workspace and read with rar_get_status().
  *  - Thread safety: calls that share a workspace must be ordered on one
  *    stream; calls on different workspaces are independent.
+ *  - Environment: RAR_TRACE (set, and not "0") makes every call print its
+ *    resolved geometry to stderr once its arguments have passed the checks
+ *    that precede the workspace check (grid, block -> channel, each channel's
+ *    range, loops and first chunk, chunk and slice sizes), and the kernel it
+ *    launches; RAR_SPIN_TIMEOUT_NS sets the default time limit of every wait
+ *    (rar_set_spin_timeout_ns overrides it).
  */
 #ifndef RAR_H
 #define RAR_H

@@ -1,0 +1,58 @@
+"""RAR_TRACE on the GPU: each call names the kernel form it launched, and the
+form follows the first-loop chunk thresholds (LL bulk from 1024 elements,
+LL128 bulk from 960, the polling forms below); the calls stay bit-exact."""
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import numpy as np, torch, oracle
+from collective_communication_gb300 import binding as B, inputs as gen
+from gpu_util import to_device, device_rows_numpy
+OP = {{"LL": oracle.LL, "LL128": oracle.LL128, "Simple": oracle.SIMPLE}}
+for n, count, proto, dtype in {cases!r}:
+    x = gen.draw("normal", n, count, 3, dtype)
+    _, send = to_device(x, dtype)
+    _, recv = to_device(x, dtype)
+    ring = list(range(n))
+    ws = B.Workspace(n, 0x1, proto, 0)
+    B.allreduce(send, recv, ring, 0x1, proto, ws, 0, 4)
+    assert B.get_status(ws) == B.Status.OK
+    want = oracle.ring_allreduce_closed(list(x), ring, 0x1, OP[proto], 0, 4)
+    got = device_rows_numpy(recv, dtype)
+    assert all(got[r].tobytes() == want[r].tobytes() for r in range(n))
+    print("case done", file=sys.stderr, flush=True)
+"""
+
+# (nranks, count, proto, dtype): one channel, so the first chunk is ceil(count / n) aligned
+CASES = [
+    (4, 4 * 1020, "LL", "f32"), (4, 4 * 1024, "LL", "f32"),
+    (4, 4 * 956, "LL128", "f32"), (4, 4 * 960, "LL128", "f32"),
+    (4, 4 * 960, "LL128", "bf16"), (4, 1 << 16, "Simple", "f32"),
+]
+WANT = [r"ring_line_kernel<float, LL, \d+>", r"ring_line_bulk_kernel<float, LL>",
+        r"ring_line_kernel<float, LL128, \d+>", r"ring_line_bulk_kernel<float, LL128>",
+        r"ring_line_bulk_kernel<bf16, LL128>", r"ring_simple_kernel<float>"]
+
+
+def test_trace_names_the_kernel_form():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    env = dict(os.environ, RAR_TRACE="1")
+    r = subprocess.run([sys.executable, "-c", SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"),
+                                                             cases=CASES)],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    kernels = [l for l in r.stderr.splitlines() if "rar trace:   kernel" in l]
+    assert len(kernels) == len(CASES), r.stderr[-2000:]
+    for line, pat in zip(kernels, WANT):
+        assert re.search(pat, line), (line, pat)
