@@ -24,6 +24,7 @@ class Status(enum.IntEnum):
     ERR_CUDA = 6
     ERR_TIMEOUT = 7
     ERR_ABORT = 8
+    ERR_BOUNDS = 9
 
 
 class Dtype(enum.IntEnum):
@@ -54,6 +55,10 @@ class RarError(RuntimeError):
 
 
 def library_path() -> str:
+    """librar.so, or with RAR_LIBRARY=debug in the environment the debug build
+    librar_debug.so (slice bounds checked on the device, RAR_ERR_BOUNDS)."""
+    if os.environ.get("RAR_LIBRARY", "") == "debug":
+        return os.path.join(HERE, "librar_debug.so")
     return os.path.join(HERE, _LIB_NAME)
 
 

@@ -451,6 +451,7 @@ const char* rar_strerror(rar_status status) {
     case RAR_ERR_CUDA: return "a CUDA runtime call failed";
     case RAR_ERR_TIMEOUT: return "a device wait ran past its time limit; the workspace is aborted";
     case RAR_ERR_ABORT: return "the workspace was aborted by an earlier failure; re-initialise it";
+    case RAR_ERR_BOUNDS: return "a slice fell outside its buffers (debug library); the workspace is aborted";
   }
   return "unknown status";
 }

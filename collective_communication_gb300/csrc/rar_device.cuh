@@ -63,12 +63,14 @@ inline int64_t workspace_bytes_for(int nranks, int nchan, int64_t buff_size) {
 constexpr uint32_t kErrWorkspace = 4;
 constexpr uint32_t kErrTimeout = 7;
 constexpr uint32_t kErrAbort = 8;
+constexpr uint32_t kErrBounds = 9;  // debug builds: a slice outside its buffers
 
 // Fault injection for tests (a wait that nothing satisfies; the wait runs out
 // of time and the launch ends with RAR_ERR_TIMEOUT).
 constexpr int kFaultNone = 0;
 constexpr int kFaultDropHead = 1;   // receivers never publish their head
 constexpr int kFaultDropAck = 2;    // staged one-shot: ranks never acknowledge their reads
+constexpr int kFaultBoundsView = 3;  // debug builds: the bounds check sees each slice one buffer further on
 
 struct RingArgs {
   const void* send[kMaxRanks];
@@ -363,6 +365,45 @@ __device__ __forceinline__ void slice_offsets(const RingArgs& a, int dense, cons
   const int64_t blk = (int64_t)rank_at_index(a, dense, c.chunk) * g.count;
   *in_off = c.offset + (g.kind == kReduceScatter ? blk : 0);
   *out_off = c.offset + (g.kind == kAllGather ? blk : 0);
+}
+
+// Debug builds (-DRAR_DEBUG): before a slice is used, check that its user
+// ranges lie inside the rank's buffers and that its bytes on the wire (a
+// binary32 bound for both types) fit its FIFO slot(s); a violation records
+// RAR_ERR_BOUNDS with the block, slice and offset in the workspace header and
+// the caller aborts instead of touching memory. Release builds: always true.
+__device__ __forceinline__ bool slice_in_bounds(const RingArgs& a, int dense, const SliceCursor& c, uint64_t rstep,
+                                                uint64_t sstep, uint64_t info) {
+#ifdef RAR_DEBUG
+  const Geometry& g = a.geo;
+  int64_t in_off, out_off;
+  slice_offsets(a, dense, c, &in_off, &out_off);
+  const int64_t N = g.nranks;
+  const int64_t in_len = g.kind == kReduceScatter ? N * g.count : g.count;
+  const int64_t out_len = g.kind == kAllGather ? N * g.count : g.count;
+  if (a.fault == kFaultBoundsView) {  // the check's own view only; the slice's accesses keep their offsets
+    in_off += in_len;
+    out_off += out_len;
+  }
+  // an empty slice touches no user memory (its offset may lie past the end)
+  bool ok = c.nelem >= 0 && (c.nelem == 0 || (in_off >= 0 && out_off >= 0 && in_off + c.nelem <= in_len &&
+                                              out_off + c.nelem <= out_len));
+  const int64_t b4 = c.nelem * 4;
+  if (g.proto == kSimple) {
+    ok = ok && b4 <= (int64_t)g.sps * g.step_bytes;
+    if (row_recvs(c.prim)) ok = ok && (int64_t)(rstep % kSteps) + g.sps <= kSteps;
+    if (row_sends(c.prim)) ok = ok && (int64_t)(sstep % kSteps) + g.sps <= kSteps;
+  } else if (g.proto == kLL) {
+    ok = ok && div_up(b4, 8) * 16 <= g.step_bytes;
+  } else {
+    ok = ok && div_up(b4, 480) * 512 <= g.step_bytes;
+  }
+  if (!ok) report_failure(header_of(a), kErrBounds, info | (11u << 24), (uint64_t)c.offset);
+  return ok;
+#else
+  (void)a; (void)dense; (void)c; (void)rstep; (void)sstep; (void)info;
+  return true;
+#endif
 }
 
 // Entry check shared by the ring kernels (thread 0): the workspace must be

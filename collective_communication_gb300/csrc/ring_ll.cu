@@ -554,7 +554,9 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   SliceCursor c;
   cursor_begin(g, dense, ring_idx, c);
   if (threadIdx.x == 0 && c.valid) {
-    if (row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24)))
+    if (!slice_in_bounds(a, dense, c, rstep, sstep, info))
+      sh_abort = 1;
+    else if (row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24)))
       sh_abort = 1;
     else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(rstep % kSteps) * step_bytes, c.prim, c.nelem, rstep,
                                       info | (9u << 24)))
@@ -575,7 +577,9 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
     const uint64_t nrstep = rstep + (row_recvs(c.prim) ? 1 : 0);
     // credit and pacing for the next step, taken while the block finishes this one
     if (threadIdx.x == 0 && nx.valid && !sh_abort) {
-      if (row_sends(nx.prim) && !wait_credit(a, cs, base_send, nsstep, &head_seen, info | (3u << 24) | (i + 1)))
+      if (!slice_in_bounds(a, dense, nx, nrstep, nsstep, info | (i + 1)))
+        sh_abort = 1;
+      else if (row_sends(nx.prim) && !wait_credit(a, cs, base_send, nsstep, &head_seen, info | (3u << 24) | (i + 1)))
         sh_abort = 1;
       else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(nrstep % kSteps) * step_bytes, nx.prim, nx.nelem,
                                         nrstep, info | (9u << 24) | (i + 1)))
@@ -1373,6 +1377,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kL8Depth, use = i / kL8Depth;
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
+      if (!sh_abort && !slice_in_bounds(a, dense, c, rstep, sstep, info | i)) sh_abort = 1;
       if (!sh_abort && row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24) | i))
         sh_abort = 1;
       mbar_arrive(&bar_ready[d]);
@@ -1386,8 +1391,14 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
     const uint64_t pol = l2_policy_evict_first();
     uint64_t rstep = base_recv;
     uint32_t gt = 0;
+    uint64_t sstep_l = base_send;  // for the debug bounds check only
     for (uint32_t i = 0; c.valid && !sh_abort; i++, cursor_next(g, c)) {
       const uint32_t d = i % kL8Depth, use = i / kL8Depth;
+      if (!slice_in_bounds(a, dense, c, rstep, sstep_l, info | i)) {
+        sh_abort = 1;
+        break;
+      }
+      if (row_sends(c.prim)) sstep_l++;
       if (!mbar_wait(a, &bar_ready[d], use & 1u, info | (6u << 24) | i) || sh_abort) {
         sh_abort = 1;
         break;

@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
+      if (!sh_abort && !slice_in_bounds(a, dense, c, rstep, sstep, info | i)) sh_abort = 1;
       if (!sh_abort && row_recvs(c.prim)) {
         Spin sp;
         while (tail_seen < rstep + sps) {
@@ -402,9 +403,15 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
     const uint64_t pol = l2_policy_evict_first();
     uint64_t rstep = base_recv;
     uint32_t gt = 0;  // tiles issued so far
+    uint64_t sstep_l = base_send;  // for the debug bounds check only
     for (uint32_t i = 0; c.valid && !sh_abort; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
       const int prim = c.prim;
+      if (!slice_in_bounds(a, dense, c, rstep, sstep_l, info | i)) {
+        sh_abort = 1;
+        break;
+      }
+      if (row_sends(prim)) sstep_l += sps;
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
       const bool vec = user_vec_ok(in + in_off, out + out_off, direct ? next_out + out_off : nullptr);

@@ -59,7 +59,8 @@ typedef enum rar_status {
   RAR_ERR_CORESIDENCY = 5, /* the (rank, channel) blocks cannot all be resident at once */
   RAR_ERR_CUDA = 6,        /* a CUDA runtime call failed */
   RAR_ERR_TIMEOUT = 7,     /* device: a wait ran past its time limit; the kernel gave up */
-  RAR_ERR_ABORT = 8        /* device: the workspace was aborted by an earlier failure */
+  RAR_ERR_ABORT = 8,       /* device: the workspace was aborted by an earlier failure */
+  RAR_ERR_BOUNDS = 9       /* device, debug library only: a slice fell outside its buffers */
 } rar_status;
 
 typedef enum rar_dtype { RAR_F32 = 0, RAR_BF16 = 1 } rar_dtype;
@@ -340,8 +341,12 @@ RAR_API void rar_set_spin_timeout_ns(uint64_t ns);
  * rar_oneshot_staged, no rank acknowledges its reads, so the fifth call's
  * guard (4 slots per rank) waits until the time limit. No GPU fault
  * happens: the waits end, every block leaves, the launch completes, and
- * rar_get_status() reports RAR_ERR_TIMEOUT. Applies to launches enqueued
- * after the call.
+ * rar_get_status() reports RAR_ERR_TIMEOUT. 3 = in the debug library
+ * (librar_debug.so) only, the device-side bounds check of the ring kernels
+ * sees every slice one buffer further on than it is (the slice's own
+ * accesses keep their offsets), so the first slice is refused and
+ * rar_get_status() reports RAR_ERR_BOUNDS; the release library ignores 3.
+ * Applies to launches enqueued after the call.
  */
 RAR_API void rar_debug_set_fault(int fault);
 
