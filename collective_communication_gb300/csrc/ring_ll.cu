@@ -599,8 +599,9 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 
 // ---------------------------------------------------------------------------
 // LL128, bulk form: the same lines, flags and head credits, with the loads of
-// large steps moved onto the TMA engine (used when chunks span at least one
-// tile). Roles as in the Simple kernel:
+// large steps moved onto the TMA engine (used from first-loop chunks of
+// kL8BulkMinChunk elements; a tile may be partial). Roles as in the Simple
+// kernel:
 //   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1);
 //                   arrives ready[i % D].
 //   warp 1, lane 0  loader: per tile of kL8TileElems elements, a pacing wait for
