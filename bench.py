@@ -576,8 +576,8 @@ def run_gpu(args):
     is_headline = (case.nranks, case.count, case.mask, case.proto, case.buff_size) == (
         default_case.nranks, default_case.count, default_case.mask, default_case.proto, default_case.buff_size)
     kernel = {"Simple": "ring_simple_kernel<float>",
-              "LL": "ring_line_bulk_kernel<float, LL> (ring_line_kernel<float, LL> for chunks < 4096)",
-              "LL128": "ring_line_bulk_kernel<float, LL128> (ring_line_kernel<float, LL128> for chunks < 3840)"}[
+              "LL": "ring_line_bulk_kernel<float, LL> (ring_line_kernel<float, LL> for chunks < 1024)",
+              "LL128": "ring_line_bulk_kernel<float, LL128> (ring_line_kernel<float, LL128> for chunks < 960)"}[
                   case.proto]
     achieved = algo / avg_launch / 1e9
     del x, y, ws
