@@ -12,7 +12,8 @@
 // shared-memory mbarriers, with the workers' loads moved onto the TMA engine:
 //   warp 0, lane 0  waiter: for slice i, waits until the receive FIFO holds it
 //                   (tail >= step + StepPerSlice) and the send FIFO has room
-//                   (head + NCCL_STEPS >= step + StepPerSlice); arrives ready[i % D].
+//                   (head + NCCL_STEPS >= step + StepPerSlice), both polled in
+//                   one loop; arrives ready[i % D].
 //   warp 1, lane 0  loader: after ready[i % D], streams the slice in tiles of
 //                   kTileElems elements: bulk copies (cp.async.bulk) of the user
 //                   input and of the received FIFO bytes into a ring of smem
@@ -21,9 +22,10 @@
 //                   memory in binary32, store the FIFO output and the user output
 //                   with 16-byte stores, release the stage (empty[stage]); after
 //                   the slice's last tile arrive done[i % D].
-//   warp 2, lane 0  poster: after ready[i % D] and done[i % D], fence.acq_rel.gpu
-//                   then publish the tail (payload first, then the tail) and the
-//                   head; arrive free[i % D] so the waiter may reuse the slot.
+//   warp 2, lane 0  poster: after ready[i % D] and done[i % D], publish the head
+//                   (the slots read), then fence.acq_rel.gpu and publish the
+//                   tail (payload first, then the tail); arrive free[i % D] so
+//                   the waiter may reuse the slot.
 // Up to D slices are in flight between waiter and poster, and up to
 // `nstages` tiles between loader and workers (about 190 KB of loads in flight
 // per SM). Empty slices still wait and post, so both ends of every connection
@@ -374,22 +376,32 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       const uint32_t d = i % kDepth, use = i / kDepth;
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
       if (!sh_abort && !slice_in_bounds(a, dense, c, rstep, sstep, info | i)) sh_abort = 1;
-      if (!sh_abort && row_recvs(c.prim)) {
-        Spin sp;
-        while (tail_seen < rstep + sps) {
+      // The slice's data (tail) and the room for what it sends (head) are
+      // polled in one loop, both loads in flight at once, so a credit that
+      // needs a poll adds no round trip after the tail. Until the receiver's
+      // first release in this call, its head may still hold the previous
+      // call's final step (< base_send): all slots free. The head is read
+      // relaxed: the receiver publishes it only after its reads of the slot
+      // have returned, and the slot is written only after the value is seen.
+      bool need_t = !sh_abort && row_recvs(c.prim) && tail_seen < rstep + sps;
+      bool need_h = !sh_abort && row_sends(c.prim) && !direct_send_row(direct, c.prim) &&  // direct sends fill no slot
+                    (head_seen > base_send ? head_seen : base_send) + kSteps < sstep + sps;
+      Spin sp;
+      while (need_t || need_h) {
+        uint64_t h = 0;
+        if (need_h) h = ld_relaxed_u64(&cs->head);
+        if (need_t) {
           tail_seen = ld_acquire_u64(&cr->tail);
-          if (tail_seen >= rstep + sps) break;
-          if (sp.poll(a, info | (2u << 24) | i, rstep + sps)) { sh_abort = 1; break; }
+          need_t = tail_seen < rstep + sps;
         }
-      }
-      if (!sh_abort && row_sends(c.prim) && !direct_send_row(direct, c.prim)) {  // direct sends fill no slot
-        Spin sp;
-        // Until the receiver's first release in this call, its head may still
-        // hold the previous call's final step (< base_send): all slots free.
-        while ((head_seen > base_send ? head_seen : base_send) + kSteps < sstep + sps) {
-          head_seen = ld_acquire_u64(&cs->head);
-          if ((head_seen > base_send ? head_seen : base_send) + kSteps >= sstep + sps) break;
-          if (sp.poll(a, info | (3u << 24) | i, sstep + sps)) { sh_abort = 1; break; }
+        if (need_h) {
+          head_seen = h > head_seen ? h : head_seen;
+          need_h = (head_seen > base_send ? head_seen : base_send) + kSteps < sstep + sps;
+        }
+        if (!(need_t || need_h)) break;
+        if (sp.poll(a, info | ((need_t ? 2u : 3u) << 24) | i, need_t ? rstep + sps : sstep + sps)) {
+          sh_abort = 1;
+          break;
         }
       }
       mbar_arrive(&bar_ready[d]);
@@ -493,14 +505,16 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
         break;
       }
       if (sh_abort) break;
+      // the head first: the slots read need no fence (their bytes have been
+      // read), and the sender waits on it
+      if (row_recvs(c.prim)) {
+        rstep += sps;
+        if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // release the slots read
+      }
       if (row_sends(c.prim)) {
         sstep += sps;
         fence_acq_rel_gpu();  // the workers' payload is visible before the tail
         st_relaxed_u64(&cs->tail, sstep);
-      }
-      if (row_recvs(c.prim)) {
-        rstep += sps;
-        if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // release the slots read
       }
       mbar_arrive(&bar_free[d]);
     }
