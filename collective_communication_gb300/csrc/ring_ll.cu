@@ -1010,7 +1010,9 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
 // there is re-polled from global memory), reduces, stores the output and
 // writes the outgoing line with one 16-byte store.
 // ---------------------------------------------------------------------------
-constexpr int kLLTileElems = 3840;
+// 8192 elements: one tile per default step (32 KiB of binary32 payload), 2 stages;
+// 1920-, 3840- and 4096-element tiles were measured slower at every size
+constexpr int kLLTileElems = 8192;
 constexpr int kLLTileLineBytes = kLLTileElems * 4 / 8 * 16;  // binary32 payload: 8 bytes per 16-byte line
 constexpr int kLLBulkMinChunk = 1024;  // chunks at least this long take the bulk form (measured: 1-8192)
 
