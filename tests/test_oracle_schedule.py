@@ -55,7 +55,7 @@ def test_schedule_counts_match_page():
 def test_schedule_brute_force(n):
     """Symbolic run of the schedule on every position of an n-ring.
 
-    - the benchmark spec form: position p handles chunk (p - s) mod n at step s,
+    - the position form: position p handles chunk (p - s) mod n at step s,
       steps counted from 1;
     - every send of position p at row s is the receive of position p+1 at row
       s+1, for the same chunk;
