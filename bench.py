@@ -46,15 +46,20 @@ def headline_case(args=None):
     from collective_communication_gb300 import inputs as gen
     nranks = getattr(args, "nranks", None) or 8
     ring = gen.ring_permutation(nranks, 3)
-    mib = getattr(args, "mib", None) or 64
+    kib = getattr(args, "kib", None) or 1024 * (getattr(args, "mib", None) or 64)
     proto = getattr(args, "proto", None) or gen.SIMPLE
     buff = getattr(args, "buff_size", None)
     if buff is None:
         buff = gen.MIB if proto == gen.SIMPLE else 0
     chans = getattr(args, "channels", None) or 12
-    name = f"n{nranks}_f32_{mib}MiB_ch{chans}_{proto}{buff // 1024 if buff else 'default'}"
-    return gen.RingCase(name, nranks, ring, (1 << chans) - 1, proto, mib * gen.MIB // 4, gen.F32, "normal", 3,
+    size = f"{kib // 1024}MiB" if kib % 1024 == 0 else f"{kib}KiB"
+    name = f"n{nranks}_f32_{size}_ch{chans}_{proto}{buff // 1024 if buff else 'default'}"
+    return gen.RingCase(name, nranks, ring, (1 << chans) - 1, proto, kib * gen.KIB // 4, gen.F32, "normal", 3,
                         buff, 4)
+
+
+def size_label(nbytes):
+    return f"{nbytes >> 20} MiB" if nbytes % (1 << 20) == 0 else f"{nbytes >> 10} KiB"
 
 
 def busbw(nbytes_per_rank, nranks, seconds):
@@ -597,7 +602,7 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"ring AllReduce, {case.nranks} virtual ranks on one GPU, f32 sum, "
-                               f"{case.bytes_per_rank >> 20} MiB per rank, ring = seeded permutation (seed 3), "
+                               f"{size_label(case.bytes_per_rank)} per rank, ring = seeded permutation (seed 3), "
                                f"{bin(case.mask).count('1')} channels, {case.proto}, "
                                f"{case.buff_size or 'default'} B FIFO, 4 chunk steps",
                    "nranks": case.nranks, "bytes_per_rank": case.bytes_per_rank, "ring_order": case.ring,
@@ -718,6 +723,7 @@ def main():
     ap.add_argument("--proto", choices=["Simple", "LL", "LL128"])
     ap.add_argument("--buff-size", type=int)
     ap.add_argument("--mib", type=int, help="MiB per rank")
+    ap.add_argument("--kib", type=int, help="KiB per rank (instead of --mib)")
     ap.add_argument("--nranks", type=int)
     ap.add_argument("--channels", type=int)
     ap.add_argument("--oneshot-tokens", type=int, help="time only the one-shot AllReduce of 7168 x T bf16")
