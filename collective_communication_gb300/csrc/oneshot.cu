@@ -138,16 +138,9 @@ __global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_c
 cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
   const int P = a.dtype == kF32 ? 4 : 8;
   const int64_t npack = a.count / P;
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
+  int device = 0, sms = 0;
+  const cudaError_t e = current_device_sms(&device, &sms);
   if (e != cudaSuccess) return e;
-  static int sm_count[64] = {0};
-  int sms = device < 64 ? sm_count[device] : 0;
-  if (sms == 0) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (e != cudaSuccess) return e;
-    if (device < 64) sm_count[device] = sms;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;

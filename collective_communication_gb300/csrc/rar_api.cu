@@ -35,6 +35,36 @@ bool trace_on() {
 }
 
 namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<uint32_t> g_setup[kMaxDevices];
+}  // namespace
+
+cudaError_t current_device_sms(int* device, int* sms) {
+  cudaError_t e = cudaGetDevice(device);
+  if (e != cudaSuccess) return e;
+  const bool cached = *device >= 0 && *device < kMaxDevices;
+  if (cached) {
+    const int v = g_sm_count[*device].load(std::memory_order_relaxed);
+    if (v != 0) {
+      *sms = v;
+      return cudaSuccess;
+    }
+  }
+  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *device);
+  if (e == cudaSuccess && cached) g_sm_count[*device].store(*sms, std::memory_order_relaxed);
+  return e;
+}
+
+bool setup_done(int device, int key) {
+  return device >= 0 && device < kMaxDevices && ((g_setup[device].load(std::memory_order_acquire) >> key) & 1u);
+}
+
+void mark_setup_done(int device, int key) {
+  if (device >= 0 && device < kMaxDevices) g_setup[device].fetch_or(1u << key, std::memory_order_release);
+}
+
+namespace {
 
 uint64_t spin_timeout_ns() {
   uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
@@ -162,16 +192,7 @@ __global__ void init_staged_header_kernel(char* ws, int nranks, int dtype, int b
 
 cudaError_t device_sms(int* sms) {
   int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  static int cache[64] = {0};
-  if (device < 64 && cache[device] != 0) {
-    *sms = cache[device];
-    return cudaSuccess;
-  }
-  e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device);
-  if (e == cudaSuccess && device < 64) cache[device] = *sms;
-  return e;
+  return current_device_sms(&device, sms);
 }
 
 __global__ void init_header_kernel(char* ws, int nranks, uint64_t mask, int proto, int64_t buff_size) {

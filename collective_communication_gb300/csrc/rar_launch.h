@@ -82,6 +82,18 @@ int staged_blocks_per_rank(int nranks, int sms);
 // Host-side tracing: RAR_TRACE set to anything but "0" in the environment
 // makes every call print its resolved geometry and kernel to stderr.
 bool trace_on();
+
+// The current device and its SM count (cached per device; safe from several
+// host threads).
+cudaError_t current_device_sms(int* device, int* sms);
+// One-time host setup per device (kernel attributes): true once `key` has
+// been marked done on `device`; mark_setup_done records it. Setting an
+// attribute twice from racing threads is harmless, so no lock is taken.
+bool setup_done(int device, int key);
+void mark_setup_done(int device, int key);
+enum SetupKey : int {
+  kSetupSimpleF32 = 0, kSetupSimpleBf16, kSetupBulkLLF32, kSetupBulkLLBf16, kSetupBulkLL128F32, kSetupBulkLL128Bf16
+};
 cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream);
 
 }  // namespace rar

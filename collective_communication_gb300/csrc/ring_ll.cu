@@ -1558,18 +1558,19 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
 }
 
 template <int PROTO>
-cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int* threads_out) {
+cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int device, int* threads_out) {
   const int nstages = f32 ? bulk_max_stages<float, PROTO>() : bulk_max_stages<uint16_t, PROTO>();
   const int smem = nstages * (f32 ? bulk_stage_bytes<float, PROTO>() : bulk_stage_bytes<uint16_t, PROTO>());
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[f32 ? 0 : 1]) {
+  const int key = PROTO == kLL ? (f32 ? kSetupBulkLLF32 : kSetupBulkLLBf16)
+                               : (f32 ? kSetupBulkLL128F32 : kSetupBulkLL128Bf16);  // the attribute is the device's
+  if (!setup_done(device, key)) {
     const cudaError_t e =
         f32 ? cudaFuncSetAttribute(ring_line_bulk_kernel<float, PROTO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    smem)
             : cudaFuncSetAttribute(ring_line_bulk_kernel<uint16_t, PROTO>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_set[f32 ? 0 : 1] = true;
+    mark_setup_done(device, key);
   }
   cfg.blockDim = dim3(kL8Threads);
   cfg.dynamicSmemBytes = (size_t)smem;
@@ -1605,15 +1606,13 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   const bool f32 = a.geo.dtype == kF32;
   const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
   int device = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  const cudaError_t e = current_device_sms(&device, &sms);
   if (e != cudaSuccess) return e;
   // LL: the bulk form from 1024-element chunks (not in the flag-wrap test
   // mode, whose slot cleanup lives in the polling form); below that the
   // polling form has the lower latency
   if (a.geo.proto == kLL && first_chunk >= kLLBulkMinChunk && grid <= sms && a.ll_flag_max == 0)
-    return launch_bulk<kLL>(a, cfg, f32, threads_out);
+    return launch_bulk<kLL>(a, cfg, f32, device, threads_out);
   if (a.geo.proto == kLL) {
     const bool small = div_up(first_chunk, f32 ? LLUnit<float>::kElems : LLUnit<uint16_t>::kElems) <=
                        8 * kThreadsSmall;
@@ -1632,7 +1631,7 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   }
   // LL128: the bulk form from 960-element chunks, the polling form (lowest
   // latency) for smaller messages.
-  if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, threads_out);
+  if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, device, threads_out);
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;
   trace_polling("LL128", f32, grid, kThreadsSmall);

@@ -569,29 +569,22 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
 // Host-side launch of the Simple kernel (declared in rar_launch.h).
 cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
   int device = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&device);
+  cudaError_t e = current_device_sms(&device, &sms);
   if (e != cudaSuccess) return e;
-  static int sm_count[64] = {0};
-  sms = device < 64 ? sm_count[device] : 0;
-  if (sms == 0) {
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    if (e != cudaSuccess) return e;
-    if (device < 64) sm_count[device] = sms;
-  }
   // One block per SM gets the deep stage ring; grids larger than the SM
   // count use two stages so that several blocks fit on an SM.
   const bool f32 = a.geo.dtype == kF32;
   const int deep = f32 ? max_stages<float>() : max_stages<uint16_t>();
   const int nstages = grid <= sms ? deep : 2;
   const int smem = nstages * (f32 ? stage_bytes<float>() : stage_bytes<uint16_t>());
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[f32 ? 0 : 1]) {
+  const int key = f32 ? kSetupSimpleF32 : kSetupSimpleBf16;  // the attribute is the device's
+  if (!setup_done(device, key)) {
     e = f32 ? cudaFuncSetAttribute(ring_simple_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    max_stages<float>() * stage_bytes<float>())
             : cudaFuncSetAttribute(ring_simple_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    max_stages<uint16_t>() * stage_bytes<uint16_t>());
     if (e != cudaSuccess) return e;
-    attr_set[f32 ? 0 : 1] = true;
+    mark_setup_done(device, key);
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
