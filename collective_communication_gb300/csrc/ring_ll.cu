@@ -1432,11 +1432,10 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
         const int64_t r_off = PROTO == kLL128 ? e0 * eb / 480 * 512 : e0 * eb / 8 * 16;
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + LB;
-        // LL128 copies the input (which does not depend on the sender) ahead
-        // of the pacing wait and the lines (measured slower for LL)
+        // the input (which does not depend on the sender) is copied ahead of
+        // the pacing wait and the lines
         const bool pace = b_rcv && (PROTO == kLL128 ? k > ready_upto : k == 0);
-        constexpr bool early = PROTO == kLL128;
-        if (early && b_in) {
+        if (b_in) {
           mbar_expect_tx(&bar_full[st], b_in);
           tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         }
@@ -1458,16 +1457,13 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
           if (paced) fence_proxy_async_global();
         }
         if (!paced) {
-          if constexpr (early) {
-            mbar_arrive_expect_tx(&bar_full[st], 0u);  // the phase completes once the input landed
-            gt++;
-          }
+          mbar_arrive_expect_tx(&bar_full[st], 0u);  // the phase completes once the input landed
+          gt++;
           sh_abort = 1;
           break;
         }
-        mbar_arrive_expect_tx(&bar_full[st], early ? b_rcv : b_in + b_rcv);
+        mbar_arrive_expect_tx(&bar_full[st], b_rcv);
         if (b_rcv) tma_load_1d(s_lines, rslot + r_off, b_rcv, &bar_full[st], pol);
-        if (!early && b_in) tma_load_1d(s_in, in + in_off + e0, b_in, &bar_full[st], pol);
         gt++;
       }
       if (has_rcv) rstep++;
