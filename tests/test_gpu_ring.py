@@ -357,3 +357,16 @@ def test_32_ranks_with_a_ring_per_channel(proto):
     check_guards(big_out, count, "f32")
     want = oracle.ring_allreduce_closed(list(x), rings, mask, OPROTO[proto], bs, 4)
     assert_bit_exact(device_rows_numpy(recv, "f32"), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("bs", [1 << 20, 4 << 20])
+def test_ll_bulk_steps_of_several_tiles(bs, dtype):
+    """LL buffers larger than the default: a step holds several 8192-element
+    tiles (2 with 1 MiB, 8 with 4 MiB), paced once per step, with a ragged
+    last loop."""
+    n, mask = 4, 0b101
+    count = 3 * n * (bs // 64) + 77
+    case = gen.RingCase("llbig", n, [2, 0, 3, 1], mask, "LL", count, dtype, "normal", 31, bs, 4)
+    x, got, _ = run_ring(case)
+    assert_bit_exact(got, oracle_full(case, x))
