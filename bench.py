@@ -267,6 +267,18 @@ def sweep(torch, B, steps, warmup, peak):
             "us": round(t * 1e6, 1),
             "roofline_frac": round(algorithmic_bytes(c, direct) / t / 1e9 / peak, 3),
             "user_bytes_frac": round(c.nranks * 2 * c.bytes_per_rank / t / 1e9 / peak, 3)}
+    # the 64 MiB workload on 1 to 19 contiguous channels (N x C blocks, one per SM;
+    # 19 x 8 = 152 uses every SM): how the ring scales with the SMs it runs on
+    scaling = {}
+    for proto, bs in ((gen.SIMPLE, gen.MIB), (gen.LL128, 0)):
+        for nch in (1, 2, 4, 8, 12, 16, 19):
+            c = gen.RingCase(f"n8_{proto}_ch{nch}", 8, cases[0].ring, (1 << nch) - 1, proto, 64 * gen.MIB // 4,
+                             gen.F32, "normal", 3, bs, 4)
+            t = statistics.median(time_ring(c, torch, B, max(3, steps // 2), 2)) / 1e3
+            scaling.setdefault(proto, {})[f"ch{nch}"] = {
+                "busbw_gbs": round(busbw(c.bytes_per_rank, c.nranks, t), 2), "us": round(t * 1e6, 1),
+                "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
+    out["channel_scaling_n8_64MiB"] = scaling
     # the halves: N=8, 12 channels, the headline's ring, 8 MiB f32 blocks (the
     # 64 MiB per-rank buffer of the AllReduce); busBW = n*block bytes / t *
     # (N-1)/N, the usual convention for these collectives
