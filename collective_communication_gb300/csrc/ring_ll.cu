@@ -604,10 +604,12 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 // kernel:
 //   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1);
 //                   arrives ready[i % D].
-//   warp 1, lane 0  loader: per tile of kL8TileElems elements, a pacing wait for
-//                   the flag of the tile's last received line (LL: of the step's
-//                   last line, once per step), then bulk copies of the tile's
-//                   received lines and user input into a smem stage.
+//   warp 1, lane 0  loader: per tile of kL8TileElems elements (LL:
+//                   kLLTileElems), a bulk copy of the tile's user input into a
+//                   smem stage as soon as the stage is free, a pacing wait for
+//                   the flag of the tile's last received line (the flags of up
+//                   to kPaceBatch tiles read together; LL: the step's last line,
+//                   once per step), then a bulk copy of the tile's received lines.
 //   warps 3..18     workers: per 4-line group, check every line's flag in
 //                   shared memory (a line that is not yet there is re-polled
 //                   from global memory until its flag matches), reduce, store
