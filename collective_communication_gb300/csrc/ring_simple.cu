@@ -14,10 +14,11 @@
 //                   (tail >= step + StepPerSlice) and the send FIFO has room
 //                   (head + NCCL_STEPS >= step + StepPerSlice), both polled in
 //                   one loop; arrives ready[i % D].
-//   warp 1, lane 0  loader: after ready[i % D], streams the slice in tiles of
-//                   kTileElems elements: bulk copies (cp.async.bulk) of the user
-//                   input and of the received FIFO bytes into a ring of smem
-//                   stages, completion counted in bytes on full[stage].
+//   warp 1, lane 0  loader: streams the slice in tiles of kTileElems elements:
+//                   bulk copies (cp.async.bulk) of the user input (the first
+//                   tile's as soon as a stage is free, before ready[i % D]) and,
+//                   after ready[i % D], of the received FIFO bytes into a ring
+//                   of smem stages, completion counted in bytes on full[stage].
 //   warps 3..10     workers: per tile, wait full[stage], reduce from shared
 //                   memory in binary32, store the FIFO output and the user output
 //                   with 16-byte stores, release the stage (empty[stage]); after
