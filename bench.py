@@ -114,14 +114,18 @@ def measured_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 200 ms while running. `load`
+    (seconds -> None), if given, keeps the GPU busy with untimed work for the
+    lead-in and lead-out of the sampling, so that the samples next to a short
+    timed region are taken under load rather than at idle."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, load=None):
         self.index = index
         self.proc = None
+        self.load = load
 
     def __enter__(self):
         try:
@@ -130,13 +134,13 @@ class ClockSampler:
                  "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        (self.load or time.sleep)(0.3)
         return self
 
     def __exit__(self, *exc):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.3)
+            (self.load or time.sleep)(0.3)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -569,7 +573,19 @@ def run_gpu(args):
     torch.cuda.synchronize()
     per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    def busy(seconds):
+        """Untimed calls on the same buffers while nvidia-smi samples around
+        the timed region (counted in no figure)."""
+        t_end = time.time() + seconds
+        while time.time() < t_end:
+            for _ in range(8):
+                step()
+            torch.cuda.synchronize()
+
+    with ClockSampler(local, load=busy) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         start.record(stream)
         for a, b in per:
             a.record(stream)
@@ -577,8 +593,8 @@ def run_gpu(args):
             b.record(stream)
         end.record(stream)
         torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
+        if world > 1:
+            dist.barrier()
     st = B.get_status(ws)
     if st != B.Status.OK:
         raise RuntimeError(f"device status {st.name}")
@@ -620,7 +636,9 @@ def run_gpu(args):
                    "nranks": case.nranks, "bytes_per_rank": case.bytes_per_rank, "ring_order": case.ring,
                    "channel_mask": hex(case.mask), "proto": case.proto, "buff_size": case.buff_size,
                    "chunk_steps": case.chunk_steps,
-                   "l2": f"inputs larger than L2 ({case.nranks} x {case.bytes_per_rank >> 20} MiB in and out per step)",
+                   "l2": f"inputs larger than L2 ({case.nranks} x {size_label(case.bytes_per_rank)} in and out per step)",
+                   "clock_sampling": "nvidia-smi every 200 ms; untimed calls keep the GPU busy for 0.3 s on each "
+                                     "side of the timed region",
                    "parallelism": f"replicas x{world} (no GPU-to-GPU data path)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3),
