@@ -23,7 +23,6 @@
 namespace rar {
 
 constexpr int kOneShotThreads = 256;
-constexpr int kOneShotUnroll = 1;  // low register count: more resident warps per SM
 
 template <typename T>
 struct OsPack;
@@ -67,71 +66,111 @@ __device__ __forceinline__ void os_store_scalar<uint16_t>(uint16_t* p, float v) 
   *p = *reinterpret_cast<uint16_t*>(&b);
 }
 
-// Peers are read in batches of kBatch ranks: every load of a batch is issued
-// before any is added, so a thread keeps kBatch x U 16-byte loads in flight;
-// the additions then run strictly in rank order.
+// Input loads of the one-shot: streamed past L1. The API refuses a receive
+// buffer that overlaps any send buffer, so no store of the kernel can meet
+// these loads and they carry no memory clobber: the compiler may issue all of
+// a pack's peer loads back to back.
+__device__ __forceinline__ uint4 os_load_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// The ragged end (fewer elements than one 16-byte pack), done by tile 0 of
+// each rank with the same rank-order sum, before the packs (so that nothing
+// of it stays live across the pack loop).
+template <typename T>
+__device__ __forceinline__ void oneshot_ragged_end(const OneShotArgs& a, int rank, int64_t npack) {
+  constexpr int P = OsPack<T>::kElems;
+  T* out = reinterpret_cast<T*>(a.recv[rank]);
+  for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kOneShotThreads) {
+    float acc = os_scalar<T>(reinterpret_cast<const T*>(a.send[0]) + e);
+    for (int q = 1; q < a.nranks; q++) acc = __fadd_rn(acc, os_scalar<T>(reinterpret_cast<const T*>(a.send[q]) + e));
+    os_store_scalar<T>(out + e, acc);
+  }
+}
+
+// Up to 8 ranks: the rank count is a template argument, so a pack's NR peer
+// loads are issued together with no per-rank guard, and the kernel fits in
+// 32 registers: 8 blocks of 256 threads (every warp slot of the SM) stay
+// resident to cover the L2 latency of the N-fold reads. (With the rank count
+// a runtime value the kernel needed about 60 registers, half the warps.)
+template <typename T, int NR>
+__global__ void __launch_bounds__(kOneShotThreads, 8) oneshot_kernel(const __grid_constant__ OneShotArgs a) {
+  constexpr int P = OsPack<T>::kElems;
+  const int rank = blockIdx.x % NR;
+  const int64_t tile = blockIdx.x / NR;
+  const int64_t ntiles = gridDim.x / NR;
+  const int64_t npack = a.count / P;
+  if (tile == 0) oneshot_ragged_end<T>(a, rank, npack);
+  for (int64_t p = tile * kOneShotThreads + threadIdx.x; p < npack; p += ntiles * kOneShotThreads) {
+    uint4 w[NR];
+#pragma unroll
+    for (int q = 0; q < NR; q++) w[q] = os_load_v4(reinterpret_cast<const T*>(a.send[q]) + p * P);
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < NR; q++) {
+      float v[8];
+      OsPack<T>::widen(w[q], v);
+#pragma unroll
+      for (int j = 0; j < P; j++) acc[j] = q == 0 ? v[j] : __fadd_rn(acc[j], v[j]);  // the sum starts at x_0
+    }
+    *reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.recv[rank]) + p * P) = OsPack<T>::narrow(acc);
+  }
+}
+
+// More than 8 ranks: peers are read in batches of kBatch, every load of a
+// batch issued before any is added; the additions run strictly in rank order.
 constexpr int kBatch = 8;
 
 template <typename T>
-__global__ void __launch_bounds__(kOneShotThreads) oneshot_kernel(const __grid_constant__ OneShotArgs a) {
+__global__ void __launch_bounds__(kOneShotThreads) oneshot_wide_kernel(const __grid_constant__ OneShotArgs a) {
   constexpr int P = OsPack<T>::kElems;
-  constexpr int U = kOneShotUnroll;
   const int N = a.nranks;
   const int rank = blockIdx.x % N;
   const int64_t tile = blockIdx.x / N;
   const int64_t ntiles = gridDim.x / N;
   const int64_t npack = a.count / P;
+  if (tile == 0) oneshot_ragged_end<T>(a, rank, npack);
   T* out = reinterpret_cast<T*>(a.recv[rank]);
-  const int64_t per_tile = (int64_t)kOneShotThreads * U;
-  for (int64_t base = tile * per_tile; base < npack; base += ntiles * per_tile) {
-    float acc[U][8];
+  for (int64_t p = tile * kOneShotThreads + threadIdx.x; p < npack; p += ntiles * kOneShotThreads) {
+    float acc[8];
     for (int q0 = 0; q0 < N; q0 += kBatch) {
-      uint4 w[kBatch][U];
+      uint4 w[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; b++)
+        if (q0 + b < N) w[b] = os_load_v4(reinterpret_cast<const T*>(a.send[q0 + b]) + p * P);
 #pragma unroll
       for (int b = 0; b < kBatch; b++) {
         if (q0 + b < N) {
-          const T* src = reinterpret_cast<const T*>(a.send[q0 + b]);
+          float v[8];
+          OsPack<T>::widen(w[b], v);
+          if (q0 + b == 0) {
 #pragma unroll
-          for (int u = 0; u < U; u++) {
-            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-            if (p < npack) w[b][u] = ld_stream_v4(src + p * P);
-          }
-        }
-      }
+            for (int j = 0; j < P; j++) acc[j] = v[j];  // the sum starts at x_0
+          } else {
 #pragma unroll
-      for (int b = 0; b < kBatch; b++) {
-        if (q0 + b < N) {
-#pragma unroll
-          for (int u = 0; u < U; u++) {
-            const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-            if (p < npack) {
-              float v[8];
-              OsPack<T>::widen(w[b][u], v);
-              if (q0 + b == 0) {
-#pragma unroll
-                for (int j = 0; j < P; j++) acc[u][j] = v[j];  // the sum starts at x_0
-              } else {
-#pragma unroll
-                for (int j = 0; j < P; j++) acc[u][j] = __fadd_rn(acc[u][j], v[j]);
-              }
-            }
+            for (int j = 0; j < P; j++) acc[j] = __fadd_rn(acc[j], v[j]);
           }
         }
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; u++) {
-      const int64_t p = base + (int64_t)u * kOneShotThreads + threadIdx.x;
-      if (p < npack) st_v4(out + p * P, OsPack<T>::narrow(acc[u]));
-    }
+    st_v4(out + p * P, OsPack<T>::narrow(acc));
   }
-  // ragged end (fewer than one 16-byte pack): tile 0 of each rank
-  if (tile == 0) {
-    for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kOneShotThreads) {
-      float acc = os_scalar<T>(reinterpret_cast<const T*>(a.send[0]) + e);
-      for (int q = 1; q < N; q++) acc = __fadd_rn(acc, os_scalar<T>(reinterpret_cast<const T*>(a.send[q]) + e));
-      os_store_scalar<T>(out + e, acc);
-    }
+}
+
+template <typename T>
+static const void* oneshot_kernel_for(int nranks) {
+  switch (nranks) {
+    case 2: return (const void*)oneshot_kernel<T, 2>;
+    case 3: return (const void*)oneshot_kernel<T, 3>;
+    case 4: return (const void*)oneshot_kernel<T, 4>;
+    case 5: return (const void*)oneshot_kernel<T, 5>;
+    case 6: return (const void*)oneshot_kernel<T, 6>;
+    case 7: return (const void*)oneshot_kernel<T, 7>;
+    case 8: return (const void*)oneshot_kernel<T, 8>;
+    default: return (const void*)oneshot_wide_kernel<T>;
   }
 }
 
@@ -143,20 +182,21 @@ cudaError_t launch_oneshot(const OneShotArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
-  const int64_t per_tile = (int64_t)kOneShotThreads * kOneShotUnroll;
-  // enough tiles to fill every SM several times over, never more than needed
-  int64_t tiles = div_up(npack, per_tile);
+  // enough tiles to fill every SM 8 blocks deep, never more than needed
+  int64_t tiles = div_up(npack, (int64_t)kOneShotThreads);
   const int64_t cap = div_up((int64_t)sms * 8, a.nranks);
   if (tiles > cap) tiles = cap;
   if (tiles < 1) tiles = 1;
   cfg.gridDim = dim3((unsigned)(tiles * a.nranks));
   cfg.blockDim = dim3(kOneShotThreads);
+  const void* fn = a.dtype == kF32 ? oneshot_kernel_for<float>(a.nranks) : oneshot_kernel_for<uint16_t>(a.nranks);
   if (trace_on())
     std::fprintf(stderr, "rar trace: oneshot nranks=%d count=%lld dtype=%s grid=%u (block b: rank b %% %d, tile b / %d) "
-                 "threads=%d kernel=oneshot_kernel\n", a.nranks, (long long)a.count, a.dtype == kF32 ? "f32" : "bf16",
-                 cfg.gridDim.x, a.nranks, a.nranks, kOneShotThreads);
-  if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_kernel<float>, a);
-  return cudaLaunchKernelEx(&cfg, oneshot_kernel<uint16_t>, a);
+                 "threads=%d kernel=%s\n", a.nranks, (long long)a.count, a.dtype == kF32 ? "f32" : "bf16",
+                 cfg.gridDim.x, a.nranks, a.nranks, kOneShotThreads,
+                 a.nranks <= 8 ? "oneshot_kernel" : "oneshot_wide_kernel");
+  void* params[] = {const_cast<OneShotArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, params);
 }
 
 }  // namespace rar
