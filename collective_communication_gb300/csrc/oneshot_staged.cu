@@ -100,7 +100,10 @@ __device__ __forceinline__ bool os_wait_at_least(const StagedArgs& a, const uint
   return true;
 }
 
-template <typename T>
+// NR > 0: the rank count as a template argument (up to 8 ranks), so that a
+// pack's NR slot loads are issued together with no per-rank guard; NR == 0:
+// any rank count, the slots read in batches of 8 ranks.
+template <typename T, int NR>
 __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_staged_kernel(const __grid_constant__ StagedArgs a) {
   constexpr int P = StPack<T>::kElems;
   constexpr int kBatchRanks = 8;
@@ -184,28 +187,43 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
     if (threadIdx.x == 0) sh_chunk[cur ^ 1] = (int64_t)atomicAdd(grab, 1ull);  // the next chunk, ahead
     const int64_t p_end = (chunk + 1) * kGrabPacks < npack ? (chunk + 1) * kGrabPacks : npack;
     for (int64_t p = chunk * kGrabPacks + threadIdx.x; p < p_end; p += kStagedThreads) {
-    float acc[8];
-    for (int q0 = 0; q0 < N; q0 += kBatchRanks) {
-      uint4 w[kBatchRanks];
+      float acc[8];
+      if constexpr (NR > 0) {
+        const char* slot0 = os_slot(a, sb, 0, s) + p * 16;
+        const int64_t rank_stride = (int64_t)kStagingSlots * sb;  // slot (q, s) to slot (q + 1, s)
+        uint4 w[NR];
 #pragma unroll
-      for (int b = 0; b < kBatchRanks; b++)
-        if (q0 + b < N) w[b] = ld_cg_v4(os_slot(a, sb, q0 + b, s) + p * 16);
+        for (int q = 0; q < NR; q++) w[q] = ld_cg_v4(slot0 + q * rank_stride);
 #pragma unroll
-      for (int b = 0; b < kBatchRanks; b++) {
-        if (q0 + b < N) {
+        for (int q = 0; q < NR; q++) {
           float v[8];
-          StPack<T>::widen(w[b], v);
-          if (q0 + b == 0) {
+          StPack<T>::widen(w[q], v);
 #pragma unroll
-            for (int k = 0; k < P; k++) acc[k] = v[k];  // the sum starts at x_0
-          } else {
+          for (int k = 0; k < P; k++) acc[k] = q == 0 ? v[k] : __fadd_rn(acc[k], v[k]);  // the sum starts at x_0
+        }
+      } else {
+        for (int q0 = 0; q0 < N; q0 += kBatchRanks) {
+          uint4 w[kBatchRanks];
 #pragma unroll
-            for (int k = 0; k < P; k++) acc[k] = __fadd_rn(acc[k], v[k]);
+          for (int b = 0; b < kBatchRanks; b++)
+            if (q0 + b < N) w[b] = ld_cg_v4(os_slot(a, sb, q0 + b, s) + p * 16);
+#pragma unroll
+          for (int b = 0; b < kBatchRanks; b++) {
+            if (q0 + b < N) {
+              float v[8];
+              StPack<T>::widen(w[b], v);
+              if (q0 + b == 0) {
+#pragma unroll
+                for (int k = 0; k < P; k++) acc[k] = v[k];  // the sum starts at x_0
+              } else {
+#pragma unroll
+                for (int k = 0; k < P; k++) acc[k] = __fadd_rn(acc[k], v[k]);
+              }
+            }
           }
         }
       }
-    }
-    st_v4(out + p * P, StPack<T>::narrow(acc));
+      st_v4(out + p * P, StPack<T>::narrow(acc));
     }
     __syncthreads();  // every thread has read sh_chunk[cur]; thread 0's next chunk is visible
   }
@@ -229,6 +247,21 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   }
 }
 
+template <typename T>
+static const void* staged_kernel_for(int nranks) {
+  switch (nranks) {
+    case 1: return (const void*)oneshot_staged_kernel<T, 1>;
+    case 2: return (const void*)oneshot_staged_kernel<T, 2>;
+    case 3: return (const void*)oneshot_staged_kernel<T, 3>;
+    case 4: return (const void*)oneshot_staged_kernel<T, 4>;
+    case 5: return (const void*)oneshot_staged_kernel<T, 5>;
+    case 6: return (const void*)oneshot_staged_kernel<T, 6>;
+    case 7: return (const void*)oneshot_staged_kernel<T, 7>;
+    case 8: return (const void*)oneshot_staged_kernel<T, 8>;
+    default: return (const void*)oneshot_staged_kernel<T, 0>;
+  }
+}
+
 int staged_blocks_per_rank(int nranks, int sms) {
   const int g = sms * kStagedBlocksPerSm / nranks;
   return g < 1 ? 1 : g;
@@ -248,8 +281,9 @@ cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream) {
     std::fprintf(stderr, "rar trace: oneshot_staged nranks=%d count=%lld dtype=%s grid=%u blocks_per_rank=%d "
                  "threads=%d kernel=oneshot_staged_kernel (cooperative)\n", a.nranks, (long long)a.count,
                  a.dtype == kF32 ? "f32" : "bf16", cfg.gridDim.x, a.blocks_per_rank, kStagedThreads);
-  if (a.dtype == kF32) return cudaLaunchKernelEx(&cfg, oneshot_staged_kernel<float>, a);
-  return cudaLaunchKernelEx(&cfg, oneshot_staged_kernel<uint16_t>, a);
+  const void* fn = a.dtype == kF32 ? staged_kernel_for<float>(a.nranks) : staged_kernel_for<uint16_t>(a.nranks);
+  void* params[] = {const_cast<StagedArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, params);
 }
 
 }  // namespace rar

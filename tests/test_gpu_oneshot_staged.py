@@ -61,6 +61,16 @@ def test_staged_ragged(n, count, dtype):
     run_staged(n, count, dtype, 20 + n)
 
 
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 32])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_staged_every_rank_count(n, dtype):
+    """Every rank count of the fixed-count kernels (1..8) and of the kernel
+    for more than 8 ranks (slots read in batches of 8), each rank's blocks
+    taking many reduce chunks, with a ragged end."""
+    ws = run_staged(n, 1300007, dtype, 80 + n)
+    run_staged(n, 1300007, dtype, 90 + n, ws=ws)  # the next slot of the same workspace
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_staged_in_place(dtype):
     for n, count in ((2, 5), (8, 7168 * 8), (5, 100003)):
