@@ -91,7 +91,7 @@ __device__ __forceinline__ void oneshot_ragged_end(const OneShotArgs& a, int ran
   }
 }
 
-// Up to 8 ranks: the rank count is a template argument, so a pack's NR peer
+// 1 to 8 ranks: the rank count is a template argument, so a pack's NR peer
 // loads are issued together with no per-rank guard, and the kernel fits in
 // 32 registers: 8 blocks of 256 threads (every warp slot of the SM) stay
 // resident to cover the L2 latency of the N-fold reads. (With the rank count
@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kOneShotThreads) oneshot_wide_kernel(const __g
 template <typename T>
 static const void* oneshot_kernel_for(int nranks) {
   switch (nranks) {
+    case 1: return (const void*)oneshot_kernel<T, 1>;
     case 2: return (const void*)oneshot_kernel<T, 2>;
     case 3: return (const void*)oneshot_kernel<T, 3>;
     case 4: return (const void*)oneshot_kernel<T, 4>;

@@ -60,10 +60,10 @@ def test_oneshot_many_tiles(n, dtype):
     run_oneshot(n, 8192 * 40 + 4096 + 24 + 3, dtype, "normal", 40 + n)
 
 
-@pytest.mark.parametrize("n", [2, 3, 4, 5, 6, 7, 8, 9, 10, 32])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 32])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_oneshot_every_rank_count(n, dtype):
-    """Every rank count of the fixed-count kernels (2..8) and of the wide
+    """Every rank count of the fixed-count kernels (1..8) and of the wide
     kernel (more than 8 ranks, peers read in batches of 8), with enough
     elements that every rank's blocks make several grid-stride passes (the
     grid holds at most 8 blocks per SM), and a ragged end."""
