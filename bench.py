@@ -52,10 +52,11 @@ def headline_case(args=None):
     if buff is None:
         buff = gen.MIB if proto == gen.SIMPLE else 0
     chans = getattr(args, "channels", None) or 12
+    dtype = getattr(args, "dtype", None) or gen.F32
     size = f"{kib // 1024}MiB" if kib % 1024 == 0 else f"{kib}KiB"
-    name = f"n{nranks}_f32_{size}_ch{chans}_{proto}{buff // 1024 if buff else 'default'}"
-    return gen.RingCase(name, nranks, ring, (1 << chans) - 1, proto, kib * gen.KIB // 4, gen.F32, "normal", 3,
-                        buff, 4)
+    name = f"n{nranks}_{dtype}_{size}_ch{chans}_{proto}{buff // 1024 if buff else 'default'}"
+    return gen.RingCase(name, nranks, ring, (1 << chans) - 1, proto, kib * gen.KIB // (4 if dtype == gen.F32 else 2),
+                        dtype, "normal", 3, buff, 4)
 
 
 def size_label(nbytes):
@@ -606,11 +607,13 @@ def run_gpu(args):
     cv = statistics.pstdev(launch_ms) / statistics.mean(launch_ms) if len(launch_ms) > 1 else 0.0
     algo = algorithmic_bytes(case)
     default_case = headline_case(None)
-    is_headline = (case.nranks, case.count, case.mask, case.proto, case.buff_size) == (
-        default_case.nranks, default_case.count, default_case.mask, default_case.proto, default_case.buff_size)
-    kernel = {"Simple": "ring_simple_kernel<float>",
-              "LL": "ring_line_bulk_kernel<float, LL> (ring_line_kernel<float, LL> for chunks < 1024)",
-              "LL128": "ring_line_bulk_kernel<float, LL128> (ring_line_kernel<float, LL128> for chunks < 960)"}[
+    is_headline = (case.nranks, case.count, case.dtype, case.mask, case.proto, case.buff_size) == (
+        default_case.nranks, default_case.count, default_case.dtype, default_case.mask, default_case.proto,
+        default_case.buff_size)
+    t = "float" if case.dtype == "f32" else "bf16"
+    kernel = {"Simple": f"ring_simple_kernel<{t}>",
+              "LL": f"ring_line_bulk_kernel<{t}, LL> (ring_line_kernel<{t}, LL> for chunks < 1024)",
+              "LL128": f"ring_line_bulk_kernel<{t}, LL128> (ring_line_kernel<{t}, LL128> for chunks < 960)"}[
                   case.proto]
     achieved = algo / avg_launch / 1e9
     del x, y, ws
@@ -628,8 +631,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "cv_per_step": round(cv, 4),
         "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"ring AllReduce, {case.nranks} virtual ranks on one GPU, f32 sum, "
+        "scaling": "weak", "vs_baseline": None, "dtype": case.dtype, "data": "synthetic",
+        "config": {"workload": f"ring AllReduce, {case.nranks} virtual ranks on one GPU, {case.dtype} sum, "
                                f"{size_label(case.bytes_per_rank)} per rank, ring = seeded permutation (seed 3), "
                                f"{bin(case.mask).count('1')} channels, {case.proto}, "
                                f"{case.buff_size or 'default'} B FIFO, 4 chunk steps",
@@ -756,6 +759,7 @@ def main():
     ap.add_argument("--kib", type=int, help="KiB per rank (instead of --mib)")
     ap.add_argument("--nranks", type=int)
     ap.add_argument("--channels", type=int)
+    ap.add_argument("--dtype", choices=["f32", "bf16"], help="element type of a named variant (default f32)")
     ap.add_argument("--oneshot-tokens", type=int, help="time only the one-shot AllReduce of 7168 x T bf16")
     ap.add_argument("--oneshot-staged", action="store_true", help="with --oneshot-tokens: the staged form")
     args = ap.parse_args()
