@@ -151,8 +151,19 @@ __global__ void __launch_bounds__(kStagedThreads, kStagedBlocksPerSm) oneshot_st
   {
     const T* src = reinterpret_cast<const T*>(a.send[rank]);
     char* dst = os_slot(a, sb, rank, s);
-    for (int64_t p = (int64_t)j * kStagedThreads + threadIdx.x; p < npack; p += (int64_t)G * kStagedThreads)
-      st_v4(dst + p * 16, ld_stream_v4(src + p * P));
+    // kCopyUnroll loads in flight per thread before their stores (one at a
+    // time, the copy was bound by the loads' latency)
+    constexpr int kCopyUnroll = 4;
+    const int64_t stride = (int64_t)G * kStagedThreads;
+    int64_t p = (int64_t)j * kStagedThreads + threadIdx.x;
+    for (; p + (kCopyUnroll - 1) * stride < npack; p += kCopyUnroll * stride) {
+      uint4 v[kCopyUnroll];
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; u++) v[u] = ld_stream_v4(src + (p + u * stride) * P);
+#pragma unroll
+      for (int u = 0; u < kCopyUnroll; u++) st_v4(dst + (p + u * stride) * 16, v[u]);
+    }
+    for (; p < npack; p += stride) st_v4(dst + p * 16, ld_stream_v4(src + p * P));
     if (j == 0)
       for (int64_t e = npack * P + threadIdx.x; e < a.count; e += kStagedThreads)
         reinterpret_cast<T*>(dst)[e] = src[e];
