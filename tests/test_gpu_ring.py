@@ -272,6 +272,23 @@ def test_line_forms_at_the_bulk_threshold(proto, thr, dtype):
         assert_bit_exact(got, oracle_full(case, x))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("buff", [4 << 10, 64 << 10, 1 << 20])
+def test_simple_sizes_follow_each_other_on_one_workspace(dtype, buff):
+    """Simple calls of very different sizes on one workspace (the step counters
+    carry over from call to call): first-loop chunks around 1024 elements,
+    ragged chunks, empty slices, one loop and many; with 4 KiB buffers
+    (512-element chunks) hundreds of loops."""
+    n = 4
+    e = 4 if dtype == "f32" else 8
+    ws = B.Workspace(n, 0b1011, "Simple", buff)
+    counts = [3 * n * 1024, 3 * n * (1024 + e), 5, 3 * n * (1024 - e) - 1, 300001, 4096, 2_000_003, 1000]
+    for k, count in enumerate(counts):
+        case = gen.RingCase("simple_alt", n, gen.RING_0231, 0b1011, "Simple", count, dtype, "normal", 90 + k, buff, 4)
+        x, got, _ = run_ring(case, workspace=ws)
+        assert_bit_exact(got, oracle_full(case, x))
+
+
 def test_too_many_blocks_is_refused():
     """32 ranks x 8 channels = 256 blocks cannot all be resident on 152 SMs:
     the cooperative launch is refused with a status, nothing hangs."""
