@@ -351,8 +351,9 @@ def sweep(torch, B, steps, warmup, peak):
             "count": c.count, "busbw_gbs": round(busbw(c.bytes_per_rank, 8, t), 2), "us": round(t * 1e6, 2),
             "roofline_frac": round(algorithmic_bytes(c) / t / 1e9 / peak, 3)}
     out["size_sweep_n8_sparse_mask_default_buffers"] = sizes
-    # one-shot bf16, N=8, 7168 x {1, 512}
-    for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1]):
+    # one-shot bf16, N=8, 7168 x {1, 512}, and the 4 KiB latency point (2048 bf16 per rank)
+    for case in (gen.oneshot_cases()[0], gen.oneshot_cases()[-1],
+                 gen.OneShotCase("oneshot_bf16_n8_4KiB", 8, 2048, gen.BF16, "normal", 1)):
         x = device_inputs(gen.RingCase(case.name, case.nranks, [], 0, "", case.count, case.dtype, "normal",
                                        case.seed), torch)
         y = rows_like(x, torch)

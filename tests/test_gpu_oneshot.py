@@ -42,7 +42,7 @@ def test_oneshot_bf16_n8(case):
     run_oneshot(case.nranks, case.count, case.dtype, case.kind, case.seed)
 
 
-@pytest.mark.parametrize("count", [1, 7, 8, 9, 1000, 4095, 123457])
+@pytest.mark.parametrize("count", [1, 7, 8, 9, 1000, 2048, 4095, 123457])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("n", [2, 3, 8, 16])
 def test_oneshot_ragged(n, count, dtype):

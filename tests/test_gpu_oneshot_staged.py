@@ -54,7 +54,7 @@ def test_staged_bf16_n8(case):
     run_staged(case.nranks, case.count, case.dtype, case.seed, kind=case.kind)
 
 
-@pytest.mark.parametrize("count", [1, 7, 8, 9, 1000, 4095, 123457])
+@pytest.mark.parametrize("count", [1, 7, 8, 9, 1000, 2048, 4095, 123457])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("n", [1, 2, 3, 8, 16])
 def test_staged_ragged(n, count, dtype):
