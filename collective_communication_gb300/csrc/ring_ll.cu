@@ -913,7 +913,12 @@ __device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char
     for (int j = 0; j < 4; j++) v[j] = j < kv ? __fadd_rn(p[j], x[j]) : 0.f;
     const uint4 wv = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), 0u, 0u);  // rounded once
     if (kv > 0) store_out_n<uint16_t>(g_out_tile + el, kv, kmax, wv);
-    for (int j = 0; j < kv; j++) fin[el + j] = (uint16_t)((j < 2 ? wv.x : wv.y) >> ((j & 1) * 16));
+    // a whole piece in one shared-memory store: el is a multiple of 4 (of 2 on
+    // a flag lane), so the 8 (4) bytes are aligned
+    if (kv == kmax && kmax == 4) *reinterpret_cast<uint2*>(fin + el) = make_uint2(wv.x, wv.y);
+    else if (kv == kmax) *reinterpret_cast<uint32_t*>(fin + el) = wv.x;
+    else
+      for (int j = 0; j < kv; j++) fin[el + j] = (uint16_t)((j < 2 ? wv.x : wv.y) >> ((j & 1) * 16));
   }
   // every worker warp passes this barrier once per owner tile, on every path;
   // the wait is bounded like every other wait of the kernel
@@ -930,9 +935,17 @@ __device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char
     const int el = (gl * 480 + L.piece_off) / 2;
     const int kv = (int)imax(0, imin(kmax, ne - el));
     uint32_t wd[4] = {0u, 0u, 0u, 0u};
+    if (kv == kmax && kmax == 8) {  // 16-byte aligned: el * 2 = 480 * gl + piece_off
+      const uint4 q = *reinterpret_cast<const uint4*>(fin + el);
+      wd[0] = q.x; wd[1] = q.y; wd[2] = q.z; wd[3] = q.w;
+    } else if (kv == kmax) {  // a flag lane's 8 bytes, 8-byte aligned
+      const uint2 q = *reinterpret_cast<const uint2*>(fin + el);
+      wd[0] = q.x; wd[1] = q.y;
+    } else {
 #pragma unroll
-    for (int j = 0; j < 8; j++)
-      if (j < kv) wd[j >> 1] |= (uint32_t)fin[el + j] << ((j & 1) * 16);
+      for (int j = 0; j < 8; j++)
+        if (j < kv) wd[j >> 1] |= (uint32_t)fin[el + j] << ((j & 1) * 16);
+    }
     uint4 pay = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     if (L.flag_lane) {
       pay.z = (uint32_t)sflag;
