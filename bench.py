@@ -34,10 +34,21 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# headline kernel from one ncu capture of this workload, for the kernel as it
-# is now (profiles/ring_simple_f32_n8_64MiB_traffic.md); None whenever the
-# kernel changes until it is captured again.
+# headline kernel from one ncu capture of this workload, and a hash of the
+# kernel sources it was captured with: when the sources differ (the kernel
+# changed since the capture) the line reports traffic null.
 TRAFFIC_BYTES_PER_LAUNCH = 1790282240
+TRAFFIC_SOURCES_SHA16 = "05f272263458d122"
+TRAFFIC_SOURCES = ("ring_simple.cu", "rar_device.cuh", "rar_geometry.h")
+
+
+def kernel_sources_sha16():
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "collective_communication_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def headline_case(args=None):
@@ -617,6 +628,7 @@ def run_gpu(args):
               "LL128": f"ring_line_bulk_kernel<{t}, LL128> (ring_line_kernel<{t}, LL128> for chunks < 960)"}[
                   case.proto]
     achieved = algo / avg_launch / 1e9
+    traffic = TRAFFIC_BYTES_PER_LAUNCH if is_headline and kernel_sources_sha16() == TRAFFIC_SOURCES_SHA16 else None
     del x, y, ws
     torch.cuda.empty_cache()
 
@@ -646,13 +658,16 @@ def run_gpu(args):
                    "parallelism": f"replicas x{world} (no GPU-to-GPU data path)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3),
-                     # the captured traffic belongs to the headline workload only
-                     "traffic": TRAFFIC_BYTES_PER_LAUNCH if is_headline else None,
+                     # the captured traffic belongs to the headline workload and
+                     # the kernel sources it was captured with only
+                     "traffic": traffic,
                      "kernel": kernel,
                      "algorithmic_bytes_per_launch": int(algo),
                      "peak_kind": f"{peak_kind} copy peak (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
-                     "user_bytes_frac": round(case.nranks * 2 * case.bytes_per_rank / avg_launch / 1e9 / peak, 3)},
+                     "user_bytes_frac": round(case.nranks * 2 * case.bytes_per_rank / avg_launch / 1e9 / peak, 3),
+                     # the measured DRAM bytes over the same launch time: what the HBM actually moved
+                     "dram_frac": round(traffic / avg_launch / 1e9 / peak, 3) if traffic else None},
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
@@ -722,7 +737,7 @@ def run_reference(args):
     def one():
         oracle.ring_allreduce_sim(list(x), case.ring, case.mask, oracle.SIMPLE, case.buff_size, case.chunk_steps)
 
-    for _ in range(min(args.warmup, 1)):
+    for _ in range(args.warmup):
         one()
     times = []
     for _ in range(args.steps):

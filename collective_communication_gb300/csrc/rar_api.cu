@@ -236,11 +236,16 @@ rar_status check_half_buffers(int kind, const void* const* send, void* const* re
   return RAR_OK;
 }
 
-// One ring collective of any kind: argument checks, ring tables, launch.
-rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
-                    rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
-                    rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, void* workspace,
-                    size_t workspaceBytes, void* stream) {
+}  // namespace
+
+// Every check of one ring call that does not involve the workspace, in the
+// order rar_allreduce reports them (operation, sizes, enums, flags, rings,
+// buffers), and the kernel arguments except the workspace fields. Enqueues
+// nothing; *grid is 0 for an empty call.
+rar_status check_ring_call(int kind, const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                           rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
+                           rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, RingArgs* a,
+                           int* grid) {
   if (op != RAR_SUM) return RAR_ERR_ARG;
   if (nranks < 2 || nranks > kMaxRanks) return RAR_ERR_ARG;
   if (count > (size_t)INT64_MAX / 4 / (size_t)nranks) return RAR_ERR_ARG;
@@ -255,16 +260,15 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
     return RAR_ERR_ARG;
   if (nrings != 1 && nrings != g.nchan) return RAR_ERR_ARG;
   if (ring_orders == nullptr) return RAR_ERR_ARG;
-  RingArgs a;
-  std::memset(&a, 0, sizeof a);
+  std::memset(a, 0, sizeof *a);
   // one ring for every channel, or one per dense channel ([C12] "GRAPH 重建：N=4")
   for (int ch = 0; ch < g.nchan; ch++) {
     int idx[kMaxRanks];
     const rar_status st = setup_ring(nranks, ring_orders + (nrings == 1 ? 0 : (size_t)ch * nranks), idx);
     if (st != RAR_OK) return st;
     for (int r = 0; r < nranks; r++) {
-      a.ring_index[ch * kMaxRanks + r] = (uint8_t)idx[r];
-      a.ring_rank[ch * kMaxRanks + idx[r]] = (uint8_t)r;
+      a->ring_index[ch * kMaxRanks + r] = (uint8_t)idx[r];
+      a->ring_rank[ch * kMaxRanks + idx[r]] = (uint8_t)r;
     }
   }
   const int64_t block = (int64_t)count * g.elem_bytes;
@@ -275,29 +279,58 @@ rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs
                                      : check_half_buffers(kind, sendbufs, recvbufs, nranks, block);
   if (st != RAR_OK) return st;
   if (trace_on()) trace_geometry(kind, g, channelMask, nrings, direct);
+  for (int r = 0; r < nranks; r++) {
+    a->send[r] = sendbufs[r];
+    a->recv[r] = recvbufs[r];
+  }
+  a->geo = g;
+  a->mask = channelMask;
+  a->conn_offset = kHeaderBytes;
+  a->fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
+  a->timeout_ns = spin_timeout_ns();
+  a->fault = g_fault.load(std::memory_order_relaxed);
+  a->ll_flag_max = g.proto == kLL ? g_ll_flag_max.load(std::memory_order_relaxed) : 0u;
+  a->direct = direct ? 1 : 0;
+  *grid = count == 0 ? 0 : nranks * g.nchan;
+  return RAR_OK;
+}
+
+rar_status launch_ring(const RingArgs& a, int grid, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = (a.geo.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr)
+                                           : launch_ring_line(a, grid, s, nullptr);
+  return from_cuda(e);
+}
+
+rar_status clear_workspace(void* workspace, int64_t clear_bytes, int nranks, uint64_t channelMask, int proto,
+                           int64_t buff_size, void* stream) {
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)clear_bytes, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  init_header_kernel<<<1, 32, 0, s>>>((char*)workspace, nranks, channelMask, proto, buff_size);
+  return from_cuda(cudaGetLastError());
+}
+
+namespace {
+
+// One ring collective of any kind: argument checks, ring tables, launch.
+rar_status run_ring(int kind, const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                    rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
+                    rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, void* workspace,
+                    size_t workspaceBytes, void* stream) {
+  RingArgs a;
+  int grid = 0;
+  rar_status st = check_ring_call(kind, sendbufs, recvbufs, nranks, count, dtype, op, ring_orders, nrings,
+                                  channelMask, proto, buffSize, chunkSteps, flags, &a, &grid);
+  if (st != RAR_OK) return st;
   if (workspace == nullptr) return RAR_ERR_WORKSPACE;
   if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
-  if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, g.nchan, g.buff_size)) return RAR_ERR_WORKSPACE;
+  if ((int64_t)workspaceBytes < workspace_bytes_for(nranks, a.geo.nchan, a.geo.buff_size)) return RAR_ERR_WORKSPACE;
   // An empty call enqueues nothing and advances no step counter ([OS89],
   // review of the empty-input case).
-  if (count == 0) return RAR_OK;
-  for (int r = 0; r < nranks; r++) {
-    a.send[r] = sendbufs[r];
-    a.recv[r] = recvbufs[r];
-  }
-  a.geo = g;
-  a.mask = channelMask;
+  if (grid == 0) return RAR_OK;
   a.ws = (char*)workspace;
-  a.conn_offset = kHeaderBytes;
-  a.fifo_offset = kHeaderBytes + conn_region_bytes(nranks, g.nchan);
-  a.timeout_ns = spin_timeout_ns();
-  a.fault = g_fault.load(std::memory_order_relaxed);
-  a.ll_flag_max = g.proto == kLL ? g_ll_flag_max.load(std::memory_order_relaxed) : 0u;
-  a.direct = direct ? 1 : 0;
-  const int grid = nranks * g.nchan;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = (g.proto == kSimple) ? launch_ring_simple(a, grid, s, nullptr) : launch_ring_line(a, grid, s, nullptr);
-  return from_cuda(e);
+  return launch_ring(a, grid, stream);
 }
 
 }  // namespace
@@ -321,11 +354,7 @@ rar_status rar_workspace_init(void* workspace, size_t workspaceBytes, int nranks
   if (((uintptr_t)workspace & 255u) != 0) return RAR_ERR_ALIGN;
   const int64_t need = workspace_bytes_for(nranks, g.nchan, g.buff_size);
   if ((int64_t)workspaceBytes < need) return RAR_ERR_WORKSPACE;
-  cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, (size_t)need, s);
-  if (e != cudaSuccess) return from_cuda(e);
-  init_header_kernel<<<1, 32, 0, s>>>((char*)workspace, nranks, channelMask, (int)proto, g.buff_size);
-  return from_cuda(cudaGetLastError());
+  return clear_workspace(workspace, need, nranks, channelMask, (int)proto, g.buff_size, stream);
 }
 
 rar_status rar_allreduce_ex(const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,

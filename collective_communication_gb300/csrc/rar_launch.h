@@ -4,9 +4,25 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include "rar.h"
 #include "rar_device.cuh"
 
 namespace rar {
+
+// ---- ring calls (rar_api.cu) ----
+// Every check of a ring call that does not involve the workspace (the codes
+// and their order are rar_allreduce's) and the kernel arguments except the
+// workspace fields; enqueues nothing. *grid is 0 for an empty call.
+rar_status check_ring_call(int kind, const void* const* sendbufs, void* const* recvbufs, int nranks, size_t count,
+                           rar_dtype dtype, rar_redop op, const int* ring_orders, int nrings, uint64_t channelMask,
+                           rar_proto proto, size_t buffSize, int chunkSteps, unsigned flags, RingArgs* a,
+                           int* grid);
+// The kernel of a checked call (a.ws set) on `stream`.
+rar_status launch_ring(const RingArgs& a, int grid, void* stream);
+// Zero the first clear_bytes of a ring workspace and write its header for
+// this configuration, on `stream`.
+rar_status clear_workspace(void* workspace, int64_t clear_bytes, int nranks, uint64_t channelMask, int proto,
+                           int64_t buff_size, void* stream);
 
 // Cooperative launch of one block per (rank, channel); grid = nranks * C.
 cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out);

@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "rar.h"
+#include "rar_launch.h"
 
 namespace {
 
@@ -51,18 +52,28 @@ extern "C" RAR_API rar_status rar_allreduce_static(const void* const* sendbufs, 
                                                    size_t count, rar_dtype dtype, rar_redop op,
                                                    const int* ring_order, uint64_t channelMask, rar_proto proto,
                                                    size_t buffSize, int chunkSteps, void* stream) {
-  const size_t need = rar_workspace_bytes(nranks, channelMask, proto, buffSize);
-  if (need == 0) return RAR_ERR_ARG;
-  if (need > (size_t)RAR_STATIC_WORKSPACE_BYTES) return RAR_ERR_WORKSPACE;
-  void* ws = nullptr;
-  rar_status st = static_ws_address(&ws);
+  // Every argument check first (rar_allreduce's codes, in its order), so
+  // that a refused call makes no CUDA call and enqueues nothing.
+  rar::RingArgs a;
+  int grid = 0;
+  rar_status st = rar::check_ring_call(rar::kAllReduce, sendbufs, recvbufs, nranks, count, dtype, op, ring_order, 1,
+                                       channelMask, proto, buffSize, chunkSteps, 0u, &a, &grid);
   if (st != RAR_OK) return st;
-  if (count > 0) {
-    // Every call starts from a cleared workspace: step counters, status,
-    // abort flag and FIFO lines of the bytes this call uses are zeroed.
-    st = rar_workspace_init(ws, need, nranks, channelMask, proto, buffSize, stream);
-    if (st != RAR_OK) return st;
-  }
-  return rar_allreduce(sendbufs, recvbufs, nranks, count, dtype, op, ring_order, channelMask, proto, buffSize,
-                       chunkSteps, ws, (size_t)RAR_STATIC_WORKSPACE_BYTES, stream);
+  const int64_t need = rar::workspace_bytes_for(nranks, a.geo.nchan, a.geo.buff_size);
+  if (need > (int64_t)RAR_STATIC_WORKSPACE_BYTES) return RAR_ERR_WORKSPACE;
+  if (grid == 0) return RAR_OK;  // an empty call: nothing to clear or run
+  void* ws = nullptr;
+  st = static_ws_address(&ws);
+  if (st != RAR_OK) return st;
+  // Every call starts from a cleared workspace: header, status, abort flag
+  // and step counters. Simple writes every FIFO byte before it reads it, so
+  // its slots need no clearing; LL and LL128 accept lines by their flags, so
+  // their FIFO lines are zeroed too (a line left by an earlier call could
+  // otherwise carry a flag this call expects).
+  const int64_t clear = a.geo.proto == rar::kSimple ? rar::kHeaderBytes + rar::conn_region_bytes(nranks, a.geo.nchan)
+                                                    : need;
+  st = rar::clear_workspace(ws, clear, nranks, channelMask, (int)proto, a.geo.buff_size, stream);
+  if (st != RAR_OK) return st;
+  a.ws = (char*)ws;
+  return rar::launch_ring(a, grid, stream);
 }

@@ -291,22 +291,26 @@ RAR_API rar_status rar_oneshot_staged(const void* const* sendbufs, void* const* 
  * have no counterpart to it. The caller still passes the send and receive
  * buffers; every other argument means what it means for rar_allreduce().
  *
- * - A call whose workspace (rar_workspace_bytes(nranks, channelMask, proto,
- *   buffSize)) would exceed RAR_STATIC_WORKSPACE_BYTES is refused with
- *   RAR_ERR_WORKSPACE and enqueues nothing; invalid arguments give the
- *   codes of rar_allreduce().
+ * - Arguments are checked first, with the codes of rar_allreduce() and in
+ *   its order; then a call whose workspace (rar_workspace_bytes(nranks,
+ *   channelMask, proto, buffSize)) would exceed RAR_STATIC_WORKSPACE_BYTES
+ *   is refused with RAR_ERR_WORKSPACE. A refused call makes no CUDA call and
+ *   enqueues nothing; so does an empty call (count 0, RAR_OK).
  * - The first call on a device looks up the array's device address on that
  *   device (it must be the current device). Make that first call before any
  *   stream capture begins.
  * - All calls share the one array, which keeps the last call's contents.
- *   Each call first clears the part it uses (step counters, status, FIFO
- *   lines) on `stream`, so no state carries over between calls.
+ *   Each call first clears, on `stream`, what it needs cleared: the header,
+ *   status and step counters, and for LL and LL128 also the FIFO lines of
+ *   the bytes it uses (Simple writes each FIFO byte before reading it). No
+ *   state carries over between calls.
  * - Calls that overlap on the GPU -- on different streams, or from threads
  *   whose calls are not ordered on one stream -- race on the array and give
  *   wrong results. Order them on one stream.
- * - Device failures are read with rar_get_status() on the array's address,
- *   which this entry point does not expose; a timed-out call leaves the
- *   array aborted only until the next call clears it.
+ * - A device failure of a call (a wait that ran out of time) cannot be read
+ *   back: the status word lives in the array, whose address this entry point
+ *   does not expose, and the next call clears it. Callers that need the
+ *   status use rar_allreduce() with a workspace of their own.
  */
 RAR_API rar_status rar_allreduce_static(const void* const* sendbufs, void* const* recvbufs,
                                         int nranks, size_t count, rar_dtype dtype, rar_redop op,

@@ -82,6 +82,40 @@ def test_argument_errors(lib):
     assert call(count=0) == S.OK
 
 
+def call_static(n=4, count=1024, dtype=B.Dtype.F32, op=0, ring=None, mask=1, proto=B.Proto.SIMPLE, bs=65536,
+                cs=4, send=None, recv=None):
+    ring = list(range(n)) if ring is None else ring
+    send = [FAKE + (i << 28) for i in range(n)] if send is None else send
+    recv = [FAKE + (1 << 35) + (i << 28) for i in range(n)] if recv is None else recv
+    L = B.load_library()
+    sp = (ctypes.c_void_p * len(send))(*send)
+    rp = (ctypes.c_void_p * len(recv))(*recv)
+    rg = (ctypes.c_int * len(ring))(*ring)
+    return L.rar_allreduce_static(sp, rp, n, count, int(dtype), op, rg, mask, int(proto), bs, cs, None)
+
+
+def test_static_argument_errors_match_and_touch_nothing(lib):
+    """rar_allreduce_static refuses bad arguments with rar_allreduce's codes
+    before any CUDA call: without a GPU any CUDA call would fail, so a code
+    other than ERR_CUDA shows that the refused call reached no CUDA call (and
+    so enqueued nothing, cleared nothing)."""
+    S = B.Status
+    bad = [dict(n=1, ring=[0]), dict(op=1), dict(dtype=7), dict(proto=9), dict(mask=0), dict(cs=8), dict(cs=3),
+           dict(bs=5000), dict(proto=B.Proto.LL128, bs=1000), dict(ring=[0, 1, 1, 2]), dict(ring=[0, 1, 2, 4]),
+           dict(send=[FAKE + 4] + [FAKE + (i << 28) for i in range(1, 4)]),
+           dict(recv=[FAKE + (1 << 28)] + [FAKE + (1 << 35) + (i << 28) for i in range(1, 4)])]
+    for kw in bad:
+        want = call(**kw)
+        assert want != S.OK
+        assert call_static(**kw) == want, kw
+    # a valid call whose workspace exceeds the array: refused before any CUDA call
+    n = 8
+    assert B.workspace_bytes(n, 0xFFF, B.Proto.SIMPLE, 1 << 20) > (16 << 20)
+    assert call_static(n=n, mask=0xFFF, bs=1 << 20) == S.ERR_WORKSPACE
+    # an empty call: nothing to do, no CUDA call
+    assert call_static(count=0) == S.OK
+
+
 def test_oneshot_argument_errors(lib):
     L = B.load_library()
     S = B.Status

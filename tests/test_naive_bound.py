@@ -1,0 +1,70 @@
+"""The naive-sum accuracy check (tests/naive_bound.py) on the oracle's ring
+results, on the CPU: the oracle's ring-order fold meets it on every element
+(f32 and bf16, N = 2..8, rings, channels and protocols as in the workloads),
+integer inputs give the naive sum exactly, and plausible mistakes fail it."""
+import numpy as np
+import pytest
+
+import oracle
+from collective_communication_gb300 import inputs as gen
+from naive_bound import bf16_key, naive_sum_f32, violations
+
+OPROTO = {"LL": oracle.LL, "LL128": oracle.LL128, "Simple": oracle.SIMPLE}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("proto", ["LL", "LL128", "Simple"])
+@pytest.mark.parametrize("n", [2, 3, 5, 8])
+def test_oracle_ring_meets_the_naive_bound(n, proto, dtype):
+    count = 200003
+    x = gen.draw("normal", n, count, 700 + n, dtype)
+    ring = gen.ring_permutation(n, 710 + n)
+    mask = gen.SPARSE_MASK
+    bs = 65536 if proto == "Simple" else 0
+    out = oracle.ring_allreduce_closed(list(x), ring, mask, OPROTO[proto], bs, 4)
+    bad, _ = violations(x, out[0], dtype)
+    assert not bad.any(), np.nonzero(bad)[0][:8]
+
+
+def test_integer_inputs_give_the_naive_sum_exactly():
+    case = gen.small_case()
+    x = case.inputs()
+    out = oracle.ring_allreduce_closed(list(x), case.ring, case.mask, oracle.SIMPLE, case.buff_size, 4)
+    assert np.array_equal(out[0], naive_sum_f32(x))
+    bad, _ = violations(x, out[0], "f32")
+    assert not bad.any()
+
+
+def test_bf16_cancellation_rule_is_needed_and_holds():
+    """Normal bf16 data with 8 ranks has elements whose sum nearly cancels:
+    there the f32 interval spans several bf16 ulps of the result, the rule
+    for them applies, and the oracle's result still meets it."""
+    n, count = 8, 1 << 20
+    x = gen.draw("normal", n, count, 720, "bf16")
+    out = oracle.ring_allreduce_closed(list(x), gen.ring_permutation(n, 3), 0xFFF, oracle.SIMPLE, 1 << 20, 4)
+    bad, wide = violations(x, out[0], "bf16")
+    assert not bad.any()
+    assert wide > 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_planted_mistakes_fail(dtype):
+    n, count = 8, 100000
+    x = gen.draw("normal", n, count, 730, dtype)
+    ring = gen.ring_permutation(n, 3)
+    good = oracle.ring_allreduce_closed(list(x), ring, 0xFFF, oracle.SIMPLE, 1 << 20, 4)[0]
+    # a dropped term: the sum of ranks 1..N-1 only
+    dropped = oracle.oneshot(list(x[1:]))[0]
+    bad, _ = violations(x, dropped, dtype)
+    assert bad.mean() > 0.9
+    # a result two or more bf16 ulps / many f32 ulps away on a few elements
+    if dtype == "f32":
+        wrong = good.copy()
+        wrong[::997] = np.nextafter(wrong[::997] * np.float32(1.0 + 2.0 ** -12), np.float32(np.inf))
+    else:
+        wrong = good.copy()
+        k = bf16_key(wrong[::997])
+        wrong[::997] = np.where(k >= 0, wrong[::997] + 2, wrong[::997] - 2).astype(np.uint16)
+    bad, _ = violations(x, wrong, dtype)
+    assert bad[::997].mean() > 0.9
+    assert not np.delete(bad, np.arange(0, count, 997)).any()

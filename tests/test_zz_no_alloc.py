@@ -1,8 +1,11 @@
 """rar_allreduce_static: the ring AllReduce entry point for callers that may not
 allocate device memory (its workspace is a fixed library array in device
-memory). Checked against rar_allreduce with a caller-allocated workspace on
-two calls in a row, through the C ABI. This file is collected last so that a
-run stopping at its first failure has already run every other test."""
+memory). Checked against rar_allreduce with a caller-allocated workspace and
+against the oracle, on two calls in a row, through the C ABI. The cases run in
+order on the one shared array: a Simple call (which clears only the header and
+step counters) follows an LL call that left its lines in the array. This file
+is collected last so that a run stopping at its first failure has already run
+every other test."""
 import ctypes
 
 import numpy as np
@@ -10,12 +13,14 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+import oracle
 from collective_communication_gb300 import binding as B
 from collective_communication_gb300 import inputs as gen
 
 pytestmark = pytest.mark.gpu
 
 STATIC_BYTES = 16 << 20  # RAR_STATIC_WORKSPACE_BYTES
+OPROTO = {"LL": oracle.LL, "LL128": oracle.LL128, "Simple": oracle.SIMPLE}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -57,6 +62,8 @@ CASES = [
     gen.RingCase("static_ll128_n4_sparse", 4, gen.RING_0231, 0b1011, gen.LL128, 123457, gen.BF16, "normal", 32,
                  256 * 1024, 4),
     gen.RingCase("static_ll_n5", 5, [4, 0, 3, 1, 2], 0b11, gen.LL, 77777, gen.F32, "normal", 33, 0, 4),
+    gen.RingCase("static_simple_n4_after_ll", 4, gen.RING_0231, 0b101, gen.SIMPLE, 200003, gen.BF16, "normal", 34,
+                 16 * 1024, 2),
 ]
 
 
@@ -78,6 +85,12 @@ def test_static_matches_allocating_entry_point(case):
         a = big_ref.view(torch.int32 if case.dtype == "f32" else torch.int16)
         b = big_out.view(torch.int32 if case.dtype == "f32" else torch.int16)
         assert bool(torch.equal(a, b)), f"call {call}: static workspace result differs"
+        want = oracle.ring_allreduce_closed(list(x), case.ring, case.mask, OPROTO[case.proto], case.buff_size,
+                                            case.chunk_steps)
+        got = b[:, :case.count].cpu().numpy()
+        for r in range(case.nranks):
+            w = want[r].view(np.int32 if case.dtype == "f32" else np.int16)
+            assert np.array_equal(got[r], w), f"call {call}, rank {r}: differs from the oracle"
 
 
 def test_static_refuses_oversized_workspace():
