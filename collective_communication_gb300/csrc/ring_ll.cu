@@ -604,7 +604,9 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 // kernel:
 //   warp 0, lane 0  waiter: send credit (head + NCCL_STEPS >= step + 1);
 //                   arrives ready[i % D].
-//   warp 1, lane 0  loader: per tile of kL8TileElems elements (LL:
+//   warp 1, lane 0  loader: per tile of 64 line groups (kL8TileElems
+//                   elements; rows that move bf16 finals and read no input
+//                   fill them with 2 * kL8TileElems elements; LL:
 //                   kLLTileElems), a bulk copy of the tile's user input into a
 //                   smem stage as soon as the stage is free, a pacing wait for
 //                   the flag of the tile's last received line (the flags of up
@@ -818,10 +820,10 @@ __device__ __forceinline__ void l8_full_store(T* p, bool flag_lane, uint4 w) {
   }
 }
 
-// Same values and lines as l8_tile_same_layout for a full tile (kL8TileElems
-// elements, all input staged): every group is whole, so the lanes need no
-// element bounds and each warp's groups are known at compile time.
-template <typename T, int PRIM>
+// Same values and lines as l8_tile_same_layout for a full tile (TE elements,
+// all input staged): every group is whole, so the lanes need no element
+// bounds and each warp's groups are known at compile time.
+template <typename T, int PRIM, int TE>
 __device__ __forceinline__ void l8_tile_full(const RingArgs& a, const char* s_lines, const char* s_in,
                                              T* g_out_tile, const char* g_rlines, char* g_slines, uint64_t rflag,
                                              uint64_t sflag, volatile int* sh_abort, uint64_t info, int w) {
@@ -831,8 +833,8 @@ __device__ __forceinline__ void l8_tile_full(const RingArgs& a, const char* s_li
   constexpr bool kOut = PRIM == kRecvReduceCopySend || PRIM == kRecvCopySend || PRIM == kRecv ||
                         PRIM == kRecvReduceCopy || PRIM == kCopySend;
   constexpr int EB = (PRIM == kSend || kRecvPartial) ? 4 : (int)sizeof(T);
-  constexpr int NG = kL8TileElems * EB / 480;
-  static_assert(kL8TileElems * EB % 480 == 0, "a tile is whole groups");
+  constexpr int NG = TE * EB / 480;
+  static_assert(TE * EB % 480 == 0 && NG <= kL8TileGroups, "a tile is whole groups of one stage");
   constexpr int GPW = (NG + kL8Warps - 1) / kL8Warps;  // groups of a warp: w, w + 16, ...
   const int gw = NG % kL8Warps == 0 || w < NG % kL8Warps ? GPW : GPW - 1;
   const LL128Lane L;
@@ -958,11 +960,12 @@ __device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char
 template <typename T>
 __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const char* s_lines, char* s_in,
                                             const T* g_in_tile, T* g_out_tile, const char* g_rlines, char* g_slines,
-                                            int ne, int covered, uint64_t rflag, uint64_t sflag,
+                                            int ne, int te, int covered, uint64_t rflag, uint64_t sflag,
                                             volatile int* sh_abort, uint64_t info, int w, uint64_t* bar_fin,
                                             uint32_t* fin_uses) {
-  if (ne == kL8TileElems && covered == ne) {
-#define RAR_L8_FULL(P) l8_tile_full<T, P>(a, s_lines, s_in, g_out_tile, g_rlines, g_slines, rflag, sflag, sh_abort, info, w)
+  if (ne == te && covered == ne) {
+#define RAR_L8_FULL(P) l8_tile_full<T, P, kL8TileElems>(a, s_lines, s_in, g_out_tile, g_rlines, g_slines, rflag, sflag, sh_abort, info, w)
+#define RAR_L8_FULL2(P) l8_tile_full<T, P, 2 * kL8TileElems>(a, s_lines, s_in, g_out_tile, g_rlines, g_slines, rflag, sflag, sh_abort, info, w)
     switch (prim) {
       case kSend: RAR_L8_FULL(kSend); return;
       case kRecvReduceSend: RAR_L8_FULL(kRecvReduceSend); return;
@@ -972,11 +975,28 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
           return;
         }
         break;  // bf16's owner row below
-      case kRecvCopySend: RAR_L8_FULL(kRecvCopySend); return;
+      case kRecvCopySend:
+        if constexpr (sizeof(T) == 2) {
+          if (te == 2 * kL8TileElems) {
+            RAR_L8_FULL2(kRecvCopySend);
+            return;
+          }
+        }
+        RAR_L8_FULL(kRecvCopySend);
+        return;
       case kRecvReduceCopy: RAR_L8_FULL(kRecvReduceCopy); return;
       case kCopySend: RAR_L8_FULL(kCopySend); return;
-      default: RAR_L8_FULL(kRecv); return;
+      default:
+        if constexpr (sizeof(T) == 2) {
+          if (te == 2 * kL8TileElems) {
+            RAR_L8_FULL2(kRecv);
+            return;
+          }
+        }
+        RAR_L8_FULL(kRecv);
+        return;
     }
+#undef RAR_L8_FULL2
 #undef RAR_L8_FULL
   }
   switch (prim) {
@@ -1033,6 +1053,16 @@ constexpr int kLLBulkMinChunk = 1024;  // chunks at least this long take the bul
 
 template <int PROTO>
 __host__ __device__ constexpr int bulk_tile_elems() { return PROTO == kLL ? kLLTileElems : kL8TileElems; }
+// Elements of a row's tile. LL128 sizes a tile by its 64 line groups: rows
+// that move bf16 finals and read no input (recvCopySend, recv) put twice the
+// elements of a binary32 row in them, so that their tiles carry as many
+// lines as the reduce-scatter rows' and the per-tile costs (pacing, stage
+// hand-off) are spread over as many bytes. Every other row: kL8TileElems.
+template <typename T, int PROTO>
+__device__ __forceinline__ int bulk_row_tile(int prim) {
+  if (PROTO == kLL128 && sizeof(T) == 2 && (prim == kRecvCopySend || prim == kRecv)) return 2 * kL8TileElems;
+  return bulk_tile_elems<PROTO>();
+}
 template <int PROTO>
 __host__ __device__ constexpr int bulk_line_bytes() { return PROTO == kLL ? kLLTileLineBytes : kL8TileGroups * 512; }
 template <typename T, int PROTO>
@@ -1311,14 +1341,14 @@ __device__ __forceinline__ bool tile_last_line_wait(const RingArgs& a, const cha
 // (bounded) for tile k itself when none does yet, or -1 if the wait gave up.
 constexpr int kPaceBatch = 8;
 __device__ __forceinline__ int l8_tiles_ready(const RingArgs& a, const char* rslot, int k, int ntiles, int64_t nelem,
-                                              int eb, uint64_t rstep, uint64_t info) {
+                                              int te, int eb, uint64_t rstep, uint64_t info) {
   uint64_t f[kPaceBatch];
 #pragma unroll
   for (int j = 0; j < kPaceBatch; j++) {
     f[j] = 0;
     if (k + j < ntiles) {
       // groups up to the end of tile k + j (each tile starts on a group boundary)
-      const int64_t g_end = div_up(imin((int64_t)(k + j + 1) * kL8TileElems, nelem) * eb, 480);
+      const int64_t g_end = div_up(imin((int64_t)(k + j + 1) * te, nelem) * eb, 480);
       f[j] = ld_relaxed_u64(reinterpret_cast<const uint64_t*>(rslot + g_end * 512 - 8));
     }
   }
@@ -1327,7 +1357,7 @@ __device__ __forceinline__ int l8_tiles_ready(const RingArgs& a, const char* rsl
   for (int j = 0; j < kPaceBatch; j++)
     if (n == j && k + j < ntiles && f[j] == rstep + 1) n = j + 1;
   if (n > 0) return k + n - 1;
-  const int64_t g_end = div_up(imin((int64_t)(k + 1) * kL8TileElems, nelem) * eb, 480);
+  const int64_t g_end = div_up(imin((int64_t)(k + 1) * te, nelem) * eb, 480);
   return tile_last_line_wait<kLL128>(a, rslot, (uint32_t)(g_end * 512), rstep, info) ? k : -1;
 }
 
@@ -1341,7 +1371,6 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
   __shared__ int sh_chan;
   __shared__ uint64_t sh_base_send, sh_base_recv;
   constexpr int P = 16 / (int)sizeof(T);
-  constexpr int TE = bulk_tile_elems<PROTO>();
   constexpr int LB = bulk_line_bytes<PROTO>();
   constexpr int SB = bulk_stage_bytes<T, PROTO>();
 
@@ -1428,7 +1457,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       const bool has_rcv = row_recvs(prim);
       const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
-      const int ntiles = (int)div_up(c.nelem, TE);
+      const int te = bulk_row_tile<T, PROTO>(prim);
+      const int ntiles = (int)div_up(c.nelem, te);
       int ready_upto = -1;  // LL128: the last tile of this step known to carry its flags
       for (int k = 0; k < ntiles; k++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
@@ -1436,8 +1466,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
           sh_abort = 1;
           break;
         }
-        const int64_t e0 = (int64_t)k * TE;
-        const int ne = (int)imin(TE, c.nelem - e0);
+        const int64_t e0 = (int64_t)k * te;
+        const int ne = (int)imin(te, c.nelem - e0);
         const int covered = ne / P * P;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
         // the tile's received lines: whole 4-line groups (LL128) or 16-byte lines (LL)
@@ -1462,7 +1492,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
         bool paced = true;
         if constexpr (PROTO == kLL128) {
           if (pace) {
-            ready_upto = l8_tiles_ready(a, rslot, k, ntiles, c.nelem, eb, rstep, info | (9u << 24) | i);
+            ready_upto = l8_tiles_ready(a, rslot, k, ntiles, c.nelem, te, eb, rstep, info | (9u << 24) | i);
             paced = ready_upto >= 0;
             if (paced) fence_proxy_async_global();
           }
@@ -1532,19 +1562,20 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
-      const int ntiles = (int)div_up(c.nelem, TE);
+      const int te = bulk_row_tile<T, PROTO>(c.prim);
+      const int ntiles = (int)div_up(c.nelem, te);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (!mbar_wait(a, &bar_full[st], su & 1u, info | (5u << 24) | i)) sh_abort = 1;
-        const int64_t e0 = (int64_t)k * TE;
-        const int ne = (int)imin(TE, c.nelem - e0);
+        const int64_t e0 = (int64_t)k * te;
+        const int ne = (int)imin(te, c.nelem - e0);
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + LB;
         if constexpr (PROTO == kLL128) {
           // the tile runs on every path so that the workers' barrier counts match
           l8_tile_any<T>(c.prim, a, s_lines, s_in, in + in_off + e0, out + out_off + e0,
-                         rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne,
+                         rslot + e0 * eb_r / 480 * 512, sslot + e0 * eb_s / 480 * 512, sh_abort ? 0 : ne, te,
                          ne / P * P, rstep + 1, sstep + 1, &sh_abort, info | (10u << 24) | i, w, &bar_fin,
                          &fin_uses);
         } else {
