@@ -513,8 +513,47 @@ __device__ __forceinline__ void line_slice(int prim, const RingArgs& a, const T*
   }
 }
 
+// Checks (thread 0) before a group of steps: the debug bounds of each of the
+// next `steps` slices from cursor c, and the send credit of the last send
+// among them; with one step per group also the pacing wait. False if a
+// check failed or a wait gave up.
 template <typename T, int PROTO, int NT>
-__global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant__ RingArgs a) {
+__device__ __forceinline__ bool line_group_checks(const RingArgs& a, const Geometry& g, int dense, SliceCursor c,
+                                                  int steps, uint64_t rstep, uint64_t sstep, ConnCounters* cs,
+                                                  uint64_t base_send, uint64_t* head_seen, const char* fifo_recv,
+                                                  uint64_t info) {
+  const SliceCursor first = c;
+  const uint64_t rstep0 = rstep;
+  uint64_t last_send = 0;
+  bool sends = false;
+  for (int k = 0; k < steps && c.valid; k++) {
+    if (!slice_in_bounds(a, dense, c, rstep, sstep, info | k)) return false;
+    if (row_sends(c.prim)) {
+      last_send = sstep++;
+      sends = true;
+    }
+    if (row_recvs(c.prim)) rstep++;
+    cursor_next(g, c);
+  }
+  if (sends && !wait_credit(a, cs, base_send, last_send, head_seen, info | (3u << 24))) return false;
+  if (steps == 1)
+    return pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(rstep0 % kSteps) * g.step_bytes, first.prim, first.nelem,
+                                   rstep0, info | (9u << 24));
+  return true;
+}
+
+// Polling form. `epoch` steps per group: 1 = the block meets at a barrier
+// after every step (head published, next step's credit and pacing checked);
+// kSteps / 2 = steps whose lines the block covers in one pass (small
+// messages): each thread then moves from step to step on its own lines, the
+// block meets only every `epoch` steps (and at the end), where it publishes
+// the head of every step read and takes the credit for the next group's
+// sends. Lines are accepted by their flags either way; the group is at most
+// half the FIFO, so no slot is written again before its reader's head covers
+// it. (With a barrier per step, the block waits at every step for its slowest
+// thread's poll.)
+template <typename T, int PROTO, int NT>
+__global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant__ RingArgs a, int epoch) {
   __shared__ volatile int sh_abort;
   __shared__ int sh_chan;
   __shared__ uint64_t sh_base_send, sh_base_recv;
@@ -553,18 +592,16 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
   uint64_t rstep = sh_base_recv, sstep = base_send, head_seen = 0;
   SliceCursor c;
   cursor_begin(g, dense, ring_idx, c);
-  if (threadIdx.x == 0 && c.valid) {
-    if (!slice_in_bounds(a, dense, c, rstep, sstep, info))
-      sh_abort = 1;
-    else if (row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24)))
-      sh_abort = 1;
-    else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(rstep % kSteps) * step_bytes, c.prim, c.nelem, rstep,
-                                      info | (9u << 24)))
-      sh_abort = 1;
-  }
+  if (threadIdx.x == 0 && c.valid &&
+      !line_group_checks<T, PROTO, NT>(a, g, dense, c, epoch, rstep, sstep, cs, base_send, &head_seen, fifo_recv,
+                                       info))
+    sh_abort = 1;
   __syncthreads();
   uint32_t i = 0;
-  while (c.valid && !sh_abort) {
+  int in_group = 0;
+  uint64_t head_published = rstep;
+  bool go = c.valid && !sh_abort;
+  while (go) {
     const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
     char* sslot = fifo_send + (int64_t)(sstep % kSteps) * step_bytes;
     int64_t in_off, out_off;
@@ -575,20 +612,39 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
     cursor_next(g, nx);
     const uint64_t nsstep = sstep + (row_sends(c.prim) ? 1 : 0);
     const uint64_t nrstep = rstep + (row_recvs(c.prim) ? 1 : 0);
-    // credit and pacing for the next step, taken while the block finishes this one
-    if (threadIdx.x == 0 && nx.valid && !sh_abort) {
-      if (!slice_in_bounds(a, dense, nx, nrstep, nsstep, info | (i + 1)))
-        sh_abort = 1;
-      else if (row_sends(nx.prim) && !wait_credit(a, cs, base_send, nsstep, &head_seen, info | (3u << 24) | (i + 1)))
-        sh_abort = 1;
-      else if (!pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(nrstep % kSteps) * step_bytes, nx.prim, nx.nelem,
-                                        nrstep, info | (9u << 24) | (i + 1)))
-        sh_abort = 1;
+    if (++in_group >= epoch || !nx.valid) {
+      int aborted;
+      if (epoch == 1) {
+        // checks and credit for the next step, taken while the block finishes this one
+        if (threadIdx.x == 0 && nx.valid && !sh_abort &&
+            !line_group_checks<T, PROTO, NT>(a, g, dense, nx, 1, nrstep, nsstep, cs, base_send, &head_seen,
+                                             fifo_recv, info | (i + 1)))
+          sh_abort = 1;
+        aborted = __syncthreads_or(sh_abort);  // the same value for every thread
+        if (threadIdx.x == 0 && !aborted && nrstep > head_published && a.fault != kFaultDropHead) {
+          st_relaxed_u64(&cr->head, nrstep);  // every thread has read this step's lines
+          head_published = nrstep;
+        }
+      } else {
+        // the head of every step read first, then the credit of the next
+        // group: a block that waits for its receiver's head has published
+        // its own, so the waits around the ring cannot close a cycle
+        aborted = __syncthreads_or(sh_abort);
+        if (threadIdx.x == 0 && !aborted) {
+          if (nrstep > head_published && a.fault != kFaultDropHead) {
+            st_relaxed_u64(&cr->head, nrstep);  // every thread has read these steps' lines
+            head_published = nrstep;
+          }
+          if (nx.valid && !line_group_checks<T, PROTO, NT>(a, g, dense, nx, epoch, nrstep, nsstep, cs, base_send,
+                                                           &head_seen, fifo_recv, info | (i + 1)))
+            sh_abort = 1;
+        }
+        if (nx.valid && !aborted) aborted = __syncthreads_or(sh_abort);
+      }
+      in_group = 0;
+      go = nx.valid && !aborted;
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && row_recvs(c.prim) && !sh_abort && a.fault != kFaultDropHead)
-      st_relaxed_u64(&cr->head, rstep + 1);  // every thread has read this step's lines
-    if (row_recvs(c.prim)) rstep++;
+    rstep = nrstep;
     sstep = nsstep;
     c = nx;
     i++;
@@ -1650,6 +1706,16 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   int device = 0, sms = 0;
   const cudaError_t e = current_device_sms(&device, &sms);
   if (e != cudaSuccess) return e;
+  // Steps per barrier group of the polling form: a group of kSteps / 2 steps
+  // when every step's lines fit one pass of the block (no pacing wait is
+  // needed) and flags do not wrap; else one step.
+  auto epoch_for = [&](int threads) -> int {
+    if (a.ll_flag_max != 0) return 1;
+    const bool one_pass = a.geo.proto == kLL
+                              ? div_up(first_chunk, f32 ? LLUnit<float>::kElems : LLUnit<uint16_t>::kElems) <= threads
+                              : div_up(first_chunk * 4, 480) <= threads / 32;
+    return one_pass ? kSteps / 2 : 1;
+  };
   // LL: the bulk form from 1024-element chunks (not in the flag-wrap test
   // mode, whose slot cleanup lives in the polling form); below that the
   // polling form has the lower latency
@@ -1662,14 +1728,16 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
       cfg.blockDim = dim3(kThreadsSmall);
       if (threads_out) *threads_out = kThreadsSmall;
       trace_polling("LL", f32, grid, kThreadsSmall);
-      return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsSmall>, a)
-                 : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsSmall>, a);
+      const int ep = epoch_for(kThreadsSmall);
+      return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsSmall>, a, ep)
+                 : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsSmall>, a, ep);
     }
     cfg.blockDim = dim3(kThreadsLarge);
     if (threads_out) *threads_out = kThreadsLarge;
     trace_polling("LL", f32, grid, kThreadsLarge);
-    return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLarge>, a)
-               : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLarge>, a);
+    const int ep = epoch_for(kThreadsLarge);
+    return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL, kThreadsLarge>, a, ep)
+               : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL, kThreadsLarge>, a, ep);
   }
   // LL128: the bulk form from 960-element chunks, the polling form (lowest
   // latency) for smaller messages.
@@ -1677,8 +1745,9 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;
   trace_polling("LL128", f32, grid, kThreadsSmall);
-  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsSmall>, a)
-             : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL128, kThreadsSmall>, a);
+  const int ep = epoch_for(kThreadsSmall);
+  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_kernel<float, kLL128, kThreadsSmall>, a, ep)
+             : cudaLaunchKernelEx(&cfg, ring_line_kernel<uint16_t, kLL128, kThreadsSmall>, a, ep);
 }
 
 }  // namespace rar

@@ -319,7 +319,7 @@ def test_too_many_blocks_is_refused():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("proto,count,bs", [("Simple", 200000, 65536), ("LL", 200000, 0),
+@pytest.mark.parametrize("proto,count,bs", [("Simple", 200000, 65536), ("LL", 200000, 0), ("LL", 200000, 4096),
                                            ("LL128", 20000, 65536), ("LL128", 400000, 131072)])
 def test_dropped_head_times_out_and_recovers(proto, count, bs):
     """Failure detection without a GPU fault: with the receivers' head
@@ -328,7 +328,9 @@ def test_dropped_head_times_out_and_recovers(proto, count, bs):
     every block leaves, the launch completes and the status reads TIMEOUT.
     Re-initialising the workspace restores normal, bit-exact operation. The
     sizes give every connection more than NCCL_STEPS steps; the two LL128
-    cases use the polling and the bulk form."""
+    cases use the polling and the bulk form, the LL case with a 4 KiB buffer
+    the polling form whose block meets every NCCL_STEPS / 2 steps (the sender
+    then waits for credit at a group boundary)."""
     case = gen.RingCase("fault", 4, gen.RING_0231, 0b11, proto, count, "f32", "normal", 8, bs, 4)
     x = case.inputs()
     _, send = to_device(x, "f32")
@@ -403,3 +405,23 @@ def test_ll_bulk_steps_of_several_tiles(bs, dtype):
     case = gen.RingCase("llbig", n, [2, 0, 3, 1], mask, "LL", count, dtype, "normal", 31, bs, 4)
     x, got, _ = run_ring(case)
     assert_bit_exact(got, oracle_full(case, x))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("bs", [4096, 8192, 16384])
+def test_ll_polling_groups_over_many_loops(bs, dtype):
+    """LL with small buffers: every step fits one pass of the block, so the
+    polling form's block meets only every NCCL_STEPS / 2 steps (heads
+    published and credits taken there); many loops per channel, several calls
+    on one workspace (step counters carry over), a ragged last loop, in place
+    on the last call."""
+    n, mask = 8, 0xFFF
+    ring = gen.ring_permutation(n, 41)
+    ws = B.Workspace(n, mask, "LL", bs)
+    for k, count in enumerate([300007, 77777, 131072 + 5]):
+        case = gen.RingCase("llgroups", n, ring, mask, "LL", count, dtype, "normal", 300 + k, bs, 4)
+        x = case.inputs()
+        want = oracle_full(case, x)
+        _, got, _ = run_ring(case, x=x, workspace=ws, in_place=(k == 2))
+        assert_bit_exact(got, want)
+        assert_naive_bound(x, got, dtype)
