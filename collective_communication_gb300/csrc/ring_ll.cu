@@ -1013,6 +1013,56 @@ __device__ __forceinline__ void l8_tile_owner_bf16(const RingArgs& a, const char
   }
 }
 
+// bf16 owner row, full tile (kL8TileElems elements, all input staged): warp
+// w takes the outgoing groups w and w + kL8Warps and, for each, the two
+// received groups 2g and 2g + 1 that hold its 240 elements; a lane rounds its
+// sums once to bf16, stores its output piece and writes the finals over its
+// own piece of the staged input (pieces are disjoint, so only this warp
+// touches these elements), and after a warp barrier the warp re-reads them
+// in the send layout. No barrier across warps.
+__device__ __forceinline__ void l8_tile_owner_bf16_full(const RingArgs& a, const char* s_lines, char* s_in,
+                                                        uint16_t* g_out_tile, const char* g_rlines, char* g_slines,
+                                                        uint64_t rflag, uint64_t sflag, volatile int* sh_abort,
+                                                        uint64_t info, int w) {
+  constexpr int NS = kL8TileElems * 2 / 480;  // outgoing groups of a tile
+  static_assert(NS % kL8Warps == 0, "whole outgoing groups per warp");
+  const LL128Lane L;
+  uint16_t* fin = reinterpret_cast<uint16_t*>(s_in);
+#pragma unroll
+  for (int q = 0; q < NS / kL8Warps; q++) {
+    const int gs = w + q * kL8Warps;
+    uint4 rv[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) rv[h] = *reinterpret_cast<const uint4*>(s_lines + (2 * gs + h) * 512 + 16 * L.lane);
+#pragma unroll
+    for (int h = 0; h < 2; h++)
+      if (!l8_accept(a, rv[h], g_rlines + (2 * gs + h) * 512 + 16 * L.lane, rflag, L.flag_lane, sh_abort, info))
+        return;  // uniform across the warp
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const int el = ((2 * gs + h) * 480 + L.piece_off) / 4;
+      float x[4];
+      l8_full_input<uint16_t, 4>(s_in, el, x);
+      const float v0 = __fadd_rn(__uint_as_float(rv[h].x), x[0]), v1 = __fadd_rn(__uint_as_float(rv[h].y), x[1]);
+      const float v2 = __fadd_rn(__uint_as_float(rv[h].z), x[2]), v3 = __fadd_rn(__uint_as_float(rv[h].w), x[3]);
+      const uint4 wv = make_uint4(pack_bf16x2(v0, v1), pack_bf16x2(v2, v3), 0u, 0u);  // rounded once
+      l8_full_store<uint16_t, 4>(g_out_tile + el, L.flag_lane, wv);
+      if (L.flag_lane) *reinterpret_cast<uint32_t*>(fin + el) = wv.x;  // 2 elements, 4-byte aligned
+      else *reinterpret_cast<uint2*>(fin + el) = make_uint2(wv.x, wv.y);  // 4 elements, 8-byte aligned
+    }
+    __syncwarp();
+    const int es = (gs * 480 + L.piece_off) / 2;
+    uint4 pay;
+    if (L.flag_lane) {
+      const uint2 f = *reinterpret_cast<const uint2*>(fin + es);  // 4 elements, 8-byte aligned
+      pay = make_uint4(f.x, f.y, (uint32_t)sflag, (uint32_t)(sflag >> 32));
+    } else {
+      pay = *reinterpret_cast<const uint4*>(fin + es);  // 8 elements, 16-byte aligned
+    }
+    st_line_v4(g_slines + gs * 512 + 16 * L.lane, pay);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const char* s_lines, char* s_in,
                                             const T* g_in_tile, T* g_out_tile, const char* g_rlines, char* g_slines,
@@ -1028,9 +1078,11 @@ __device__ __forceinline__ void l8_tile_any(int prim, const RingArgs& a, const c
       case kRecvReduceCopySend:
         if constexpr (sizeof(T) == 4) {
           RAR_L8_FULL(kRecvReduceCopySend);
-          return;
+        } else {
+          l8_tile_owner_bf16_full(a, s_lines, s_in, reinterpret_cast<uint16_t*>(g_out_tile), g_rlines, g_slines,
+                                  rflag, sflag, sh_abort, info, w);
         }
-        break;  // bf16's owner row below
+        return;
       case kRecvCopySend:
         if constexpr (sizeof(T) == 2) {
           if (te == 2 * kL8TileElems) {
