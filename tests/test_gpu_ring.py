@@ -425,3 +425,19 @@ def test_ll_polling_groups_over_many_loops(bs, dtype):
         _, got, _ = run_ring(case, x=x, workspace=ws, in_place=(k == 2))
         assert_bit_exact(got, want)
         assert_naive_bound(x, got, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_ll_polling_one_pass_of_1024_threads(dtype):
+    """LL steps of 257..512 units (first-loop chunks of 514..1022 f32
+    elements, below the bulk form's 1024): the polling form runs 1024 threads
+    so that a step is one pass, with barrier groups; two calls on one
+    workspace, the second ragged."""
+    n, mask = 8, 0xFFF
+    ring = gen.ring_permutation(n, 43)
+    ws = B.Workspace(n, mask, "LL", 0)
+    for k, count in enumerate([65536, 12 * 8 * 1000 + 7]):
+        case = gen.RingCase("ll1024", n, ring, mask, "LL", count, dtype, "normal", 310 + k, 0, 4)
+        x, got, _ = run_ring(case, workspace=ws)
+        assert_bit_exact(got, oracle_full(case, x))
+        assert_naive_bound(x, got, dtype)
