@@ -45,12 +45,21 @@ struct WsHeader {
 // head: steps the receiver has released; tail: steps the sender has published
 // (Simple), or the sender's step count at the end of a call (LL, LL128). Each
 // on its own 128-byte line so that the two sides' polls do not share a line.
+// head_h1 / tail_h1: the same counters of the second half of a connection
+// whose steps a split LL128 launch moves with two blocks per (rank, channel)
+// (each half a fixed element range of every step). Every call ends with both
+// halves' counters at the call's final step, so that any form may follow.
 struct ConnCounters {
   uint64_t head;
-  uint64_t pad0[15];
+  uint64_t pad0[7];
+  uint64_t head_h1;
+  uint64_t pad0b[7];
   uint64_t tail;
-  uint64_t pad1[15];
+  uint64_t pad1[7];
+  uint64_t tail_h1;
+  uint64_t pad1b[7];
 };
+static_assert(sizeof(ConnCounters) == 256, "one connection's counters fill kConnBytes");
 
 inline int64_t conn_region_bytes(int nranks, int nchan) {
   return align_up((int64_t)nranks * nchan * kConnBytes, 4096);
@@ -304,6 +313,9 @@ __device__ __forceinline__ bool mbar_wait(const RingArgs& a, uint64_t* bar, uint
 __device__ __forceinline__ ConnCounters* conn_at(const RingArgs& a, int dense_channel, int edge) {
   return (ConnCounters*)(a.ws + a.conn_offset) + ((int64_t)dense_channel * a.geo.nranks + edge);
 }
+// The head / tail of half `half` of a connection (0 unless a launch splits it).
+__device__ __forceinline__ uint64_t* conn_head(ConnCounters* c, int half) { return half ? &c->head_h1 : &c->head; }
+__device__ __forceinline__ uint64_t* conn_tail(ConnCounters* c, int half) { return half ? &c->tail_h1 : &c->tail; }
 __device__ __forceinline__ char* fifo_at(const RingArgs& a, int dense_channel, int edge) {
   return a.ws + a.fifo_offset + ((int64_t)dense_channel * a.geo.nranks + edge) * a.geo.buff_size;
 }
@@ -312,15 +324,18 @@ __device__ __forceinline__ char* fifo_at(const RingArgs& a, int dense_channel, i
 // the (b % C)-th set bit of the mask; each thread below 64 tests one bit the
 // way the page's kernel entry does: n = popcount(mask & ((1 << id) - 1))
 // ([C23] "Kernel 如何把 Block 映射到 Channel").
-__device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* dense, int* sh_chan_id) {
+__device__ __forceinline__ void map_block_index(const RingArgs& a, int b, int* rank, int* dense, int* sh_chan_id) {
   int C = a.geo.nchan;
-  *rank = blockIdx.x / C;
-  *dense = blockIdx.x % C;
+  *rank = b / C;
+  *dense = b % C;
   int tid = threadIdx.x;
   if (tid < kMaxChannels && ((a.mask >> tid) & 1ull)) {
     uint64_t below = tid == 0 ? 0ull : (a.mask & ((1ull << tid) - 1ull));
     if (__popcll(below) == *dense) *sh_chan_id = tid;
   }
+}
+__device__ __forceinline__ void map_block(const RingArgs& a, int* rank, int* dense, int* sh_chan_id) {
+  map_block_index(a, (int)blockIdx.x, rank, dense, sh_chan_id);
 }
 
 // Ring index of user rank `rank` on dense channel `dense`, and the user rank

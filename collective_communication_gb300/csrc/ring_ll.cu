@@ -414,15 +414,37 @@ __device__ __forceinline__ void ll128_owner_bf16(const RingArgs& a, const uint16
 // ---------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------
-__device__ __noinline__ bool wait_credit(const RingArgs& a, ConnCounters* cs, uint64_t base_send, uint64_t step,
+__device__ __noinline__ bool wait_credit(const RingArgs& a, const uint64_t* head, uint64_t base_send, uint64_t step,
                                          uint64_t* head_seen, uint64_t info) {
   Spin sp;
   while (true) {
     const uint64_t h = *head_seen > base_send ? *head_seen : base_send;
     if (h + kSteps >= step + 1) return true;
-    *head_seen = ld_acquire_u64(&cs->head);
+    *head_seen = ld_acquire_u64(head);
     const uint64_t h2 = *head_seen > base_send ? *head_seen : base_send;
     if (h2 + kSteps >= step + 1) return true;
+    if (sp.poll(a, info, step + 1)) return false;
+  }
+}
+
+// Send credit of a split connection: both halves of the receiver must have
+// released the slot. (Each step's split point follows the step's size, so a
+// later step in the same slot can give one half lines that the other half's
+// receiver read in the earlier step.)
+__device__ __noinline__ bool wait_credit_both(const RingArgs& a, ConnCounters* cs, uint64_t base_send, uint64_t step,
+                                              uint64_t (&seen)[2], uint64_t info) {
+  Spin sp;
+  auto ok = [&]() {
+    const uint64_t h0 = seen[0] > base_send ? seen[0] : base_send;
+    const uint64_t h1 = seen[1] > base_send ? seen[1] : base_send;
+    return (h0 < h1 ? h0 : h1) + kSteps >= step + 1;
+  };
+  while (true) {
+    if (ok()) return true;
+    const uint64_t h0 = ld_acquire_u64(&cs->head), h1 = ld_acquire_u64(&cs->head_h1);
+    seen[0] = h0 > seen[0] ? h0 : seen[0];
+    seen[1] = h1 > seen[1] ? h1 : seen[1];
+    if (ok()) return true;
     if (sp.poll(a, info, step + 1)) return false;
   }
 }
@@ -535,7 +557,7 @@ __device__ __forceinline__ bool line_group_checks(const RingArgs& a, const Geome
     if (row_recvs(c.prim)) rstep++;
     cursor_next(g, c);
   }
-  if (sends && !wait_credit(a, cs, base_send, last_send, head_seen, info | (3u << 24))) return false;
+  if (sends && !wait_credit(a, &cs->head, base_send, last_send, head_seen, info | (3u << 24))) return false;
   if (steps == 1)
     return pace_wait<T, PROTO, NT>(a, fifo_recv + (int64_t)(rstep0 % kSteps) * g.step_bytes, first.prim, first.nelem,
                                    rstep0, info | (9u << 24));
@@ -649,8 +671,14 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
     c = nx;
     i++;
   }
-  // the sender's step count carries over to the next call
-  if (threadIdx.x == 0 && !sh_abort) st_relaxed_u64(&cs->tail, sstep);
+  // the sender's step count carries over to the next call; the counters of
+  // the second half of a split connection follow (no block of this launch
+  // moves that half)
+  if (threadIdx.x == 0 && !sh_abort) {
+    st_relaxed_u64(&cs->tail, sstep);
+    st_relaxed_u64(&cs->tail_h1, sstep);
+    st_relaxed_u64(&cr->head_h1, rstep);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1473,7 +1501,24 @@ __device__ __forceinline__ int l8_tiles_ready_f(const RingArgs& a, const char* r
   return tile_last_line_wait<kLL128>(a, rslot, (uint32_t)(g_end * 512), rstep, info) ? k : -1;
 }
 
-template <typename T, int PROTO>
+// Elements [lo, hi) of a step of ne elements that half `half` of a split
+// launch moves: the first half rounded up to whole 4-line groups of bf16
+// payload (240 elements, two groups of binary32), so that both halves start
+// on a group boundary whichever type a row's lines carry, and a row's
+// received and sent lines of one half cover the same elements.
+constexpr int kSplitAlign = 240;
+__device__ __forceinline__ void split_range(int64_t ne, int half, int nsplit, int64_t* lo, int64_t* hi) {
+  if (nsplit == 1) {
+    *lo = 0;
+    *hi = ne;
+    return;
+  }
+  const int64_t m = imin(ne, div_up(ne, 2 * kSplitAlign) * kSplitAlign);
+  *lo = half ? m : 0;
+  *hi = half ? ne : m;
+}
+
+template <typename T, int PROTO, int SPLIT>
 __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __grid_constant__ RingArgs a,
                                                                         int nstages) {
   extern __shared__ __align__(128) char smem[];
@@ -1489,18 +1534,24 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
   const Geometry& g = a.geo;
   if (threadIdx.x == 0) sh_chan = -1;
   __syncthreads();
+  // blocks [0, N * C) move the first half of every step (all of it unless
+  // the launch splits), blocks [N * C, 2 * N * C) the second half
+  const int nblk = g.nranks * g.nchan;
+  const int half = SPLIT == 1 ? 0 : (int)blockIdx.x / nblk;
   int rank, dense;
-  map_block(a, &rank, &dense, &sh_chan);
+  map_block_index(a, SPLIT == 1 ? (int)blockIdx.x : (int)blockIdx.x % nblk, &rank, &dense, &sh_chan);
   __syncthreads();
   const int N = g.nranks;
   const int ring_idx = ring_index_of(a, dense, rank);
   const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
   ConnCounters* cs = conn_at(a, dense, e_send);
   ConnCounters* cr = conn_at(a, dense, e_recv);
+  uint64_t* r_head = conn_head(cr, half);  // this block's releases
+  uint64_t* s_tail = conn_tail(cs, half);
   char* fifo_send = fifo_at(a, dense, e_send);
   const char* fifo_recv = fifo_at(a, dense, e_recv);
   if (threadIdx.x == 0) {
-    const uint64_t tail0 = ld_relaxed_u64(&cs->tail), head0 = ld_relaxed_u64(&cr->head);  // with the header
+    const uint64_t tail0 = ld_relaxed_u64(s_tail), head0 = ld_relaxed_u64(r_head);  // with the header
     sh_abort = entry_check(a) ? 0 : 1;
     for (int d = 0; d < kL8Depth; d++) {
       mbar_init(&bar_ready[d], 1);
@@ -1512,7 +1563,8 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       mbar_init(&bar_empty[st], kL8Warps);
     }
     mbar_init(&bar_fin, kL8Warps);
-    // Both counters belong to this block and equal the previous call's final step.
+    // Both counters belong to this block (this half) and equal the previous
+    // call's final step.
     sh_base_send = tail0;
     sh_base_recv = head0;
     reinterpret_cast<uint8_t*>(a.ws + kTraceOffset)[blockIdx.x] = (uint8_t)sh_chan;
@@ -1533,12 +1585,19 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
     if (lane != 0) return;
     // ---- waiter ----
     uint64_t rstep = base_recv, sstep = base_send, head_seen = 0;
+    uint64_t seen2[2] = {0, 0};  // split launches: both halves' heads
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kL8Depth, use = i / kL8Depth;
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
       if (!sh_abort && !slice_in_bounds(a, dense, c, rstep, sstep, info | i)) sh_abort = 1;
-      if (!sh_abort && row_sends(c.prim) && !wait_credit(a, cs, base_send, sstep, &head_seen, info | (3u << 24) | i))
-        sh_abort = 1;
+      if (!sh_abort && row_sends(c.prim)) {
+        bool ok;
+        if constexpr (SPLIT == 1)
+          ok = wait_credit(a, &cs->head, base_send, sstep, &head_seen, info | (3u << 24) | i);
+        else
+          ok = wait_credit_both(a, cs, base_send, sstep, seen2, info | (3u << 24) | i);
+        if (!ok) sh_abort = 1;
+      }
       mbar_arrive(&bar_ready[d]);
       if (sh_abort) break;
       if (row_recvs(c.prim)) rstep++;
@@ -1570,20 +1629,24 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       const int eb = row_recvs_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       const int te = bulk_row_tile<T, PROTO>(prim);
-      const int ntiles = (int)div_up(c.nelem, te);
+      int64_t lo, hi;
+      split_range(c.nelem, half, SPLIT, &lo, &hi);
+      const int64_t nh = hi - lo;
+      const char* rslot_h = rslot + lo * eb / 480 * 512;  // LL128 only (lo is 0 for LL)
+      const int ntiles = (int)div_up(nh, te);
       int ready_upto = -1;  // LL128: the last tile of this step known to carry its flags
       for (int k = 0; k < ntiles; k++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         uint64_t pf[kPaceBatch];
         if constexpr (PROTO == kLL128) {
-          if (has_rcv && k > ready_upto) l8_flags_issue(rslot, k, ntiles, c.nelem, te, eb, pf);
+          if (has_rcv && k > ready_upto) l8_flags_issue(rslot_h, k, ntiles, nh, te, eb, pf);
         }
         if (su > 0 && !mbar_wait(a, &bar_empty[st], (su - 1) & 1u, info | (7u << 24) | i)) {
           sh_abort = 1;
           break;
         }
-        const int64_t e0 = (int64_t)k * te;
-        const int ne = (int)imin(te, c.nelem - e0);
+        const int64_t e0 = lo + (int64_t)k * te;
+        const int ne = (int)imin(te, hi - e0);
         const int covered = ne / P * P;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
         // the tile's received lines: whole 4-line groups (LL128) or 16-byte lines (LL)
@@ -1608,7 +1671,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
         bool paced = true;
         if constexpr (PROTO == kLL128) {
           if (pace) {
-            ready_upto = l8_tiles_ready_f(a, rslot, k, ntiles, c.nelem, te, eb, rstep, info | (9u << 24) | i, pf);
+            ready_upto = l8_tiles_ready_f(a, rslot_h, k, ntiles, nh, te, eb, rstep, info | (9u << 24) | i, pf);
             paced = ready_upto >= 0;
             if (paced) fence_proxy_async_global();
           }
@@ -1654,12 +1717,20 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       }
       if (row_recvs(c.prim)) {
         rstep++;
-        if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // every line of the step was read
+        if (a.fault != kFaultDropHead) st_relaxed_u64(r_head, rstep);  // every line of this half was read
       }
       if (row_sends(c.prim)) sstep++;
       mbar_arrive(&bar_free[d]);
     }
-    if (!aborted) st_relaxed_u64(&cs->tail, sstep);  // the sender's step count carries over to the next call
+    if (!aborted) {
+      // the sender's step count carries over to the next call; without a
+      // split, the second half's counters follow
+      st_relaxed_u64(s_tail, sstep);
+      if (SPLIT == 1) {
+        st_relaxed_u64(&cs->tail_h1, sstep);
+        st_relaxed_u64(&cr->head_h1, rstep);
+      }
+    }
   } else {
     // ---- workers ----
     const int w = warp - 3;
@@ -1679,13 +1750,15 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
       const int te = bulk_row_tile<T, PROTO>(c.prim);
-      const int ntiles = (int)div_up(c.nelem, te);
+      int64_t lo, hi;
+      split_range(c.nelem, half, SPLIT, &lo, &hi);
+      const int ntiles = (int)div_up(hi - lo, te);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
         if (!mbar_wait(a, &bar_full[st], su & 1u, info | (5u << 24) | i)) sh_abort = 1;
-        const int64_t e0 = (int64_t)k * te;
-        const int ne = (int)imin(te, c.nelem - e0);
+        const int64_t e0 = lo + (int64_t)k * te;
+        const int ne = (int)imin(te, hi - e0);
         char* s_lines = smem + (int64_t)st * SB;
         char* s_in = s_lines + LB;
         if constexpr (PROTO == kLL128) {
@@ -1715,29 +1788,32 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
   }
 }
 
-template <int PROTO>
+template <int PROTO, int SPLIT>
 cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int device, int* threads_out) {
   const int nstages = f32 ? bulk_max_stages<float, PROTO>() : bulk_max_stages<uint16_t, PROTO>();
   const int smem = nstages * (f32 ? bulk_stage_bytes<float, PROTO>() : bulk_stage_bytes<uint16_t, PROTO>());
   const int key = PROTO == kLL ? (f32 ? kSetupBulkLLF32 : kSetupBulkLLBf16)
-                               : (f32 ? kSetupBulkLL128F32 : kSetupBulkLL128Bf16);  // the attribute is the device's
+                  : SPLIT == 1 ? (f32 ? kSetupBulkLL128F32 : kSetupBulkLL128Bf16)
+                               : (f32 ? kSetupBulkLL128F32Split : kSetupBulkLL128Bf16Split);  // per device
   if (!setup_done(device, key)) {
-    const cudaError_t e =
-        f32 ? cudaFuncSetAttribute(ring_line_bulk_kernel<float, PROTO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   smem)
-            : cudaFuncSetAttribute(ring_line_bulk_kernel<uint16_t, PROTO>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t e = f32 ? cudaFuncSetAttribute(ring_line_bulk_kernel<float, PROTO, SPLIT>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                              : cudaFuncSetAttribute(ring_line_bulk_kernel<uint16_t, PROTO, SPLIT>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     mark_setup_done(device, key);
   }
+  cfg.gridDim = dim3(cfg.gridDim.x * (unsigned)SPLIT);
   cfg.blockDim = dim3(kL8Threads);
   cfg.dynamicSmemBytes = (size_t)smem;
   if (threads_out) *threads_out = kL8Threads;
   if (trace_on())
-    std::fprintf(stderr, "rar trace:   kernel ring_line_bulk_kernel<%s, %s> grid %u threads %d stages %d smem %d\n",
-                 f32 ? "float" : "bf16", PROTO == kLL ? "LL" : "LL128", cfg.gridDim.x, kL8Threads, nstages, smem);
-  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<float, PROTO>, a, nstages)
-             : cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<uint16_t, PROTO>, a, nstages);
+    std::fprintf(stderr,
+                 "rar trace:   kernel ring_line_bulk_kernel<%s, %s> grid %u threads %d stages %d smem %d split %d\n",
+                 f32 ? "float" : "bf16", PROTO == kLL ? "LL" : "LL128", cfg.gridDim.x, kL8Threads, nstages, smem,
+                 SPLIT);
+  return f32 ? cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<float, PROTO, SPLIT>, a, nstages)
+             : cudaLaunchKernelEx(&cfg, ring_line_bulk_kernel<uint16_t, PROTO, SPLIT>, a, nstages);
 }
 
 void trace_polling(const char* proto, bool f32, int grid, int threads) {
@@ -1780,7 +1856,7 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   // mode, whose slot cleanup lives in the polling form); below that the
   // polling form has the lower latency
   if (a.geo.proto == kLL && first_chunk >= kLLBulkMinChunk && grid <= sms && a.ll_flag_max == 0)
-    return launch_bulk<kLL>(a, cfg, f32, device, threads_out);
+    return launch_bulk<kLL, 1>(a, cfg, f32, device, threads_out);
   if (a.geo.proto == kLL) {
     // 256 threads when a step is one pass of them; larger steps take 1024
     // threads, so that a step is still one pass (barrier groups: at 256 KiB
@@ -1806,7 +1882,15 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   }
   // LL128: the bulk form from 960-element chunks, the polling form (lowest
   // latency) for smaller messages.
-  if (first_chunk >= kL8BulkMinChunk && grid <= sms) return launch_bulk<kLL128>(a, cfg, f32, device, threads_out);
+  // Two blocks per (rank, channel), each a fixed half of every step, when
+  // twice the grid still fits one block per SM: the bulk form is bound by
+  // its blocks' instruction issue, and a mask of few channels leaves SMs idle
+  // (not in the flag-wrap test mode, whose slot cleanup lives in the polling
+  // form anyway).
+  if (first_chunk >= kL8BulkMinChunk && grid <= sms) {
+    if (2 * grid <= sms && a.ll_flag_max == 0) return launch_bulk<kLL128, 2>(a, cfg, f32, device, threads_out);
+    return launch_bulk<kLL128, 1>(a, cfg, f32, device, threads_out);
+  }
   cfg.blockDim = dim3(kThreadsSmall);
   if (threads_out) *threads_out = kThreadsSmall;
   trace_polling("LL128", f32, grid, kThreadsSmall);
