@@ -1632,7 +1632,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       int64_t lo, hi;
       split_range(c.nelem, half, SPLIT, &lo, &hi);
       const int64_t nh = hi - lo;
-      const char* rslot_h = rslot + lo * eb / 480 * 512;  // LL128 only (lo is 0 for LL)
+      const char* rslot_h = rslot + (PROTO == kLL128 ? lo * eb / 480 * 512 : lo * eb / 8 * 16);  // the half's lines
       const int ntiles = (int)div_up(nh, te);
       int ready_upto = -1;  // LL128: the last tile of this step known to carry its flags
       for (int k = 0; k < ntiles; k++) {
@@ -1676,7 +1676,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
             if (paced) fence_proxy_async_global();
           }
         } else if (pace) {
-          paced = tile_last_line_wait<PROTO>(a, rslot, (uint32_t)div_up(c.nelem * eb, 8) * 16u, rstep,
+          paced = tile_last_line_wait<PROTO>(a, rslot_h, (uint32_t)div_up(nh * eb, 8) * 16u, rstep,
                                              info | (9u << 24) | i);
           if (paced) fence_proxy_async_global();
         }
@@ -1792,6 +1792,7 @@ template <int PROTO, int SPLIT>
 cudaError_t launch_bulk(const RingArgs& a, cudaLaunchConfig_t cfg, bool f32, int device, int* threads_out) {
   const int nstages = f32 ? bulk_max_stages<float, PROTO>() : bulk_max_stages<uint16_t, PROTO>();
   const int smem = nstages * (f32 ? bulk_stage_bytes<float, PROTO>() : bulk_stage_bytes<uint16_t, PROTO>());
+  static_assert(PROTO == kLL128 || SPLIT == 1, "only LL128's bulk form splits");
   const int key = PROTO == kLL ? (f32 ? kSetupBulkLLF32 : kSetupBulkLLBf16)
                   : SPLIT == 1 ? (f32 ? kSetupBulkLL128F32 : kSetupBulkLL128Bf16)
                                : (f32 ? kSetupBulkLL128F32Split : kSetupBulkLL128Bf16Split);  // per device
@@ -1855,6 +1856,8 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   // LL: the bulk form from 1024-element chunks (not in the flag-wrap test
   // mode, whose slot cleanup lives in the polling form); below that the
   // polling form has the lower latency
+  // (one block per (rank, channel): LL's steps are one tile each, paced
+  // once per step, and a split over two blocks measured no faster)
   if (a.geo.proto == kLL && first_chunk >= kLLBulkMinChunk && grid <= sms && a.ll_flag_max == 0)
     return launch_bulk<kLL, 1>(a, cfg, f32, device, threads_out);
   if (a.geo.proto == kLL) {

@@ -66,12 +66,14 @@ def test_trace_names_the_kernel_form():
         assert re.search(pat, line), (line, pat)
 
 
-def test_trace_reports_the_ll128_split():
-    """4 ranks on 1 channel and 8 ranks on the sparse 8-channel mask (64
-    blocks) split; 8 ranks on 12 channels (96 blocks: 192 do not fit 152 SMs)
-    do not."""
+def test_trace_reports_the_bulk_split():
+    """LL128's bulk form: 4 ranks on 1 channel and 8 ranks on the sparse
+    8-channel mask (64 blocks) split; 8 ranks on 12 channels (96 blocks: 192
+    do not fit 152 SMs) do not. LL's bulk form never splits."""
     cases = [(4, 4 * 2000, "LL128", "f32", 0x1), (8, 8 * 8 * 2000 + 13, "LL128", "bf16", 0b101101011011),
-             (8, 8 * 12 * 2000, "LL128", "f32", 0xFFF)]
-    want = [(r"grid 8 ", "split 2"), (r"grid 128 ", "split 2"), (r"grid 96 ", "split 1")]
+             (8, 8 * 12 * 2000, "LL128", "f32", 0xFFF), (4, 4 * 2048, "LL", "f32", 0x1),
+             (8, 8 * 12 * 2048, "LL", "bf16", 0xFFF)]
+    want = [(r"grid 8 ", "split 2"), (r"grid 128 ", "split 2"), (r"grid 96 ", "split 1"), (r"grid 4 ", "split 1"),
+            (r"grid 96 ", "split 1")]
     for line, (grid, split) in zip(_kernel_lines(cases), want):
         assert "ring_line_bulk_kernel" in line and re.search(grid, line) and line.rstrip().endswith(split), line
