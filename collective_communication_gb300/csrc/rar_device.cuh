@@ -313,6 +313,23 @@ __device__ __forceinline__ bool mbar_wait(const RingArgs& a, uint64_t* bar, uint
 __device__ __forceinline__ ConnCounters* conn_at(const RingArgs& a, int dense_channel, int edge) {
   return (ConnCounters*)(a.ws + a.conn_offset) + ((int64_t)dense_channel * a.geo.nranks + edge);
 }
+// Elements [lo, hi) of a slice of ne elements that part `half` of a launch
+// split over two blocks per (rank, channel) moves: the first part rounded up
+// to a multiple of `align` elements (the protocol's layout unit), the rest to
+// the second. Both ends of a connection compute the same split from the same
+// slice.
+__device__ __forceinline__ void split_range(int64_t ne, int half, int nsplit, int64_t align, int64_t* lo,
+                                            int64_t* hi) {
+  if (nsplit == 1) {
+    *lo = 0;
+    *hi = ne;
+    return;
+  }
+  const int64_t m = imin(ne, div_up(ne, 2 * align) * align);
+  *lo = half ? m : 0;
+  *hi = half ? ne : m;
+}
+
 // The head / tail of half `half` of a connection (0 unless a launch splits it).
 __device__ __forceinline__ uint64_t* conn_head(ConnCounters* c, int half) { return half ? &c->head_h1 : &c->head; }
 __device__ __forceinline__ uint64_t* conn_tail(ConnCounters* c, int half) { return half ? &c->tail_h1 : &c->tail; }

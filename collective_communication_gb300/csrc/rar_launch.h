@@ -109,7 +109,7 @@ bool setup_done(int device, int key);
 void mark_setup_done(int device, int key);
 enum SetupKey : int {
   kSetupSimpleF32 = 0, kSetupSimpleBf16, kSetupBulkLLF32, kSetupBulkLLBf16, kSetupBulkLL128F32, kSetupBulkLL128Bf16,
-  kSetupBulkLL128F32Split, kSetupBulkLL128Bf16Split
+  kSetupBulkLL128F32Split, kSetupBulkLL128Bf16Split, kSetupSimpleF32Split, kSetupSimpleBf16Split
 };
 cudaError_t launch_oneshot_staged(const StagedArgs& a, cudaStream_t stream);
 

@@ -1501,22 +1501,11 @@ __device__ __forceinline__ int l8_tiles_ready_f(const RingArgs& a, const char* r
   return tile_last_line_wait<kLL128>(a, rslot, (uint32_t)(g_end * 512), rstep, info) ? k : -1;
 }
 
-// Elements [lo, hi) of a step of ne elements that half `half` of a split
-// launch moves: the first half rounded up to whole 4-line groups of bf16
-// payload (240 elements, two groups of binary32), so that both halves start
-// on a group boundary whichever type a row's lines carry, and a row's
-// received and sent lines of one half cover the same elements.
+// The split point of LL128's bulk form: whole 4-line groups of bf16 payload
+// (240 elements, two groups of binary32), so that both parts start on a group
+// boundary whichever type a row's lines carry, and a row's received and sent
+// lines of one part cover the same elements.
 constexpr int kSplitAlign = 240;
-__device__ __forceinline__ void split_range(int64_t ne, int half, int nsplit, int64_t* lo, int64_t* hi) {
-  if (nsplit == 1) {
-    *lo = 0;
-    *hi = ne;
-    return;
-  }
-  const int64_t m = imin(ne, div_up(ne, 2 * kSplitAlign) * kSplitAlign);
-  *lo = half ? m : 0;
-  *hi = half ? ne : m;
-}
 
 template <typename T, int PROTO, int SPLIT>
 __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __grid_constant__ RingArgs a,
@@ -1630,7 +1619,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
       const int te = bulk_row_tile<T, PROTO>(prim);
       int64_t lo, hi;
-      split_range(c.nelem, half, SPLIT, &lo, &hi);
+      split_range(c.nelem, half, SPLIT, kSplitAlign, &lo, &hi);
       const int64_t nh = hi - lo;
       const char* rslot_h = rslot + (PROTO == kLL128 ? lo * eb / 480 * 512 : lo * eb / 8 * 16);  // the half's lines
       const int ntiles = (int)div_up(nh, te);
@@ -1751,7 +1740,7 @@ __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __g
       slice_offsets(a, dense, c, &in_off, &out_off);
       const int te = bulk_row_tile<T, PROTO>(c.prim);
       int64_t lo, hi;
-      split_range(c.nelem, half, SPLIT, &lo, &hi);
+      split_range(c.nelem, half, SPLIT, kSplitAlign, &lo, &hi);
       const int ntiles = (int)div_up(hi - lo, te);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {

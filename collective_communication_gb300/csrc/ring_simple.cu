@@ -309,7 +309,11 @@ __device__ __forceinline__ bool user_vec_ok(const T* in, const T* out, const T* 
   return (((uintptr_t)in | (uintptr_t)out | (uintptr_t)next) & 15u) == 0;
 }
 
-template <typename T>
+// Split point of the Simple kernel's two-block form: 16 elements keep every
+// part's user and FIFO bytes 16-byte aligned for both element types.
+constexpr int kSimpleSplitAlign = 16;
+
+template <typename T, int SPLIT>
 __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __grid_constant__ RingArgs a,
                                                                         int nstages) {
   extern __shared__ __align__(128) char smem[];
@@ -324,19 +328,26 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   const Geometry& g = a.geo;
   if (threadIdx.x == 0) sh_chan = -1;
   __syncthreads();
+  // blocks [0, N * C) move the first part of every slice (all of it unless
+  // the launch splits), blocks [N * C, 2 * N * C) the rest
+  const int nblk = g.nranks * g.nchan;
+  const int half = SPLIT == 1 ? 0 : (int)blockIdx.x / nblk;
   int rank, dense;
-  map_block(a, &rank, &dense, &sh_chan);
+  map_block_index(a, SPLIT == 1 ? (int)blockIdx.x : (int)blockIdx.x % nblk, &rank, &dense, &sh_chan);
   __syncthreads();
   const int N = g.nranks;
   const int ring_idx = ring_index_of(a, dense, rank);
   const int e_send = ring_idx, e_recv = (ring_idx + N - 1) % N;
   ConnCounters* cs = conn_at(a, dense, e_send);
   ConnCounters* cr = conn_at(a, dense, e_recv);
+  uint64_t* s_tail = conn_tail(cs, half);  // this part's published steps
+  const uint64_t* r_tail = conn_tail(cr, half);
+  uint64_t* r_head = conn_head(cr, half);
   char* fifo_send = fifo_at(a, dense, e_send);
   const char* fifo_recv = fifo_at(a, dense, e_recv);
 
   if (threadIdx.x == 0) {
-    const uint64_t tail0 = ld_relaxed_u64(&cs->tail), head0 = ld_relaxed_u64(&cr->head);  // with the header
+    const uint64_t tail0 = ld_relaxed_u64(s_tail), head0 = ld_relaxed_u64(r_head);  // with the header
     sh_abort = entry_check(a) ? 0 : 1;
     for (int d = 0; d < kDepth; d++) {
       mbar_init(&bar_ready[d], 1);
@@ -372,7 +383,17 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
   if (warp == 0) {
     if (lane != 0) return;
     // ---- waiter ----
-    uint64_t rstep = base_recv, sstep = base_send, tail_seen = 0, head_seen = 0;
+    uint64_t rstep = base_recv, sstep = base_send, tail_seen = 0, head_seen = 0, head_seen1 = 0;
+    // the send credit: the receiver's head (both parts' heads when the launch
+    // splits: each slice's split point follows its size, so a later slice in
+    // the same slot can give one part bytes that the other part's receiver
+    // read before)
+    auto credit = [&]() -> uint64_t {
+      const uint64_t h0 = head_seen > base_send ? head_seen : base_send;
+      if (SPLIT == 1) return h0;
+      const uint64_t h1 = head_seen1 > base_send ? head_seen1 : base_send;
+      return h0 < h1 ? h0 : h1;
+    };
     for (uint32_t i = 0; c.valid; i++, cursor_next(g, c)) {
       const uint32_t d = i % kDepth, use = i / kDepth;
       if (use > 0 && !mbar_wait(a, &bar_free[d], (use - 1) & 1u, info | (1u << 24) | i)) sh_abort = 1;
@@ -386,18 +407,22 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       // have returned, and the slot is written only after the value is seen.
       bool need_t = !sh_abort && row_recvs(c.prim) && tail_seen < rstep + sps;
       bool need_h = !sh_abort && row_sends(c.prim) && !direct_send_row(direct, c.prim) &&  // direct sends fill no slot
-                    (head_seen > base_send ? head_seen : base_send) + kSteps < sstep + sps;
+                    credit() + kSteps < sstep + sps;
       Spin sp;
       while (need_t || need_h) {
-        uint64_t h = 0;
-        if (need_h) h = ld_relaxed_u64(&cs->head);
+        uint64_t h = 0, h1 = 0;
+        if (need_h) {
+          h = ld_relaxed_u64(&cs->head);
+          if (SPLIT == 2) h1 = ld_relaxed_u64(&cs->head_h1);
+        }
         if (need_t) {
-          tail_seen = ld_acquire_u64(&cr->tail);
+          tail_seen = ld_acquire_u64(r_tail);
           need_t = tail_seen < rstep + sps;
         }
         if (need_h) {
           head_seen = h > head_seen ? h : head_seen;
-          need_h = (head_seen > base_send ? head_seen : base_send) + kSteps < sstep + sps;
+          head_seen1 = h1 > head_seen1 ? h1 : head_seen1;
+          need_h = credit() + kSteps < sstep + sps;
         }
         if (!(need_t || need_h)) break;
         if (sp.poll(a, info | ((need_t ? 2u : 3u) << 24) | i, need_t ? rstep + sps : sstep + sps)) {
@@ -436,7 +461,9 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       const bool rcv_bytes = has_rcv && !(rcv_own_out && prim == kRecv);
       const int rcv_eb = recv_is_partial(prim) ? 4 : (int)sizeof(T);
       const char* rslot = fifo_recv + (int64_t)(rstep % kSteps) * step_bytes;
-      const int ntiles = (int)div_up(c.nelem, kTileElems);
+      int64_t lo, hi;
+      split_range(c.nelem, half, SPLIT, kSimpleSplitAlign, &lo, &hi);
+      const int ntiles = (int)div_up(hi - lo, kTileElems);
       // The slice's first tile copies its input as soon as a stage is free,
       // before the wait for the slice's tail and credit (the input does not
       // depend on the peers; copying it early takes its HBM latency off the
@@ -453,8 +480,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
           sh_abort = 1;
           break;
         }
-        const int64_t e0 = (int64_t)k * kTileElems;
-        const int ne = (int)imin(kTileElems, c.nelem - e0);
+        const int64_t e0 = lo + (int64_t)k * kTileElems;
+        const int ne = (int)imin(kTileElems, hi - e0);
         const int covered = vec ? ne / P * P : 0;
         const uint32_t b_in = has_in ? (uint32_t)covered * (uint32_t)sizeof(T) : 0u;
         const uint32_t b_rcv = rcv_bytes ? (uint32_t)covered * (uint32_t)rcv_eb : 0u;
@@ -510,14 +537,20 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       // read), and the sender waits on it
       if (row_recvs(c.prim)) {
         rstep += sps;
-        if (a.fault != kFaultDropHead) st_relaxed_u64(&cr->head, rstep);  // release the slots read
+        if (a.fault != kFaultDropHead) st_relaxed_u64(r_head, rstep);  // release the slots read
       }
       if (row_sends(c.prim)) {
         sstep += sps;
         fence_acq_rel_gpu();  // the workers' payload is visible before the tail
-        st_relaxed_u64(&cs->tail, sstep);
+        st_relaxed_u64(s_tail, sstep);
       }
       mbar_arrive(&bar_free[d]);
+    }
+    // without a split, the second part's counters follow this call's final
+    // steps (a later split call starts both parts from them)
+    if (SPLIT == 1 && !sh_abort) {
+      st_relaxed_u64(&cs->tail_h1, sstep);
+      st_relaxed_u64(&cr->head_h1, rstep);
     }
   } else {
     // ---- workers ----
@@ -539,7 +572,9 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
       int64_t in_off, out_off;
       slice_offsets(a, dense, c, &in_off, &out_off);
       const bool vec = user_vec_ok(in + in_off, out + out_off, direct ? next_out + out_off : nullptr);
-      const int ntiles = (int)div_up(c.nelem, kTileElems);
+      int64_t lo, hi;
+      split_range(c.nelem, half, SPLIT, kSimpleSplitAlign, &lo, &hi);
+      const int ntiles = (int)div_up(hi - lo, kTileElems);
       bool stop = false;
       for (int k = 0; k < ntiles; k++, gt++) {
         const uint32_t st = gt % nstages, su = gt / nstages;
@@ -547,8 +582,8 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
           stop = true;
           break;
         }
-        const int64_t e0 = (int64_t)k * kTileElems;
-        const int ne = (int)imin(kTileElems, c.nelem - e0);
+        const int64_t e0 = lo + (int64_t)k * kTileElems;
+        const int ne = (int)imin(kTileElems, hi - e0);
         const char* s_in = smem + (int64_t)st * SB;
         const char* s_rcv = s_in + kTileElems * (int)sizeof(T);
         tile_compute_any<T>(direct, c.prim, s_in, s_rcv, in + in_off, out + out_off, next_out + out_off, rslot,
@@ -568,6 +603,27 @@ __global__ void __launch_bounds__(kSimpleThreads, 1) ring_simple_kernel(const __
 }
 
 // Host-side launch of the Simple kernel (declared in rar_launch.h).
+template <typename T, int SPLIT>
+cudaError_t launch_simple_form(const RingArgs& a, cudaLaunchConfig_t cfg, int device, int nstages, int smem,
+                               int key) {
+  if (!setup_done(device, key)) {
+    const cudaError_t e = cudaFuncSetAttribute(ring_simple_kernel<T, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               max_stages<T>() * stage_bytes<T>());
+    if (e != cudaSuccess) return e;
+    mark_setup_done(device, key);
+  }
+  cfg.gridDim = dim3(cfg.gridDim.x * (unsigned)SPLIT);
+  if (trace_on())
+    std::fprintf(stderr, "rar trace:   kernel ring_simple_kernel<%s> grid %u threads %d stages %d smem %d split %d\n",
+                 sizeof(T) == 4 ? "float" : "bf16", cfg.gridDim.x, kSimpleThreads, nstages, smem, SPLIT);
+  return cudaLaunchKernelEx(&cfg, ring_simple_kernel<T, SPLIT>, a, nstages);
+}
+
+// First-loop chunks of at least this many elements split a grid that fits the
+// SMs twice over two blocks per (rank, channel); smaller messages keep one
+// block per pair (their time is the hand-off chain, not the SMs' stores).
+constexpr int64_t kSimpleSplitMinChunk = 65536;
+
 cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream, int* threads_out) {
   int device = 0, sms = 0;
   cudaError_t e = current_device_sms(&device, &sms);
@@ -578,15 +634,11 @@ cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream,
   const int deep = f32 ? max_stages<float>() : max_stages<uint16_t>();
   const int nstages = grid <= sms ? deep : 2;
   const int smem = nstages * (f32 ? stage_bytes<float>() : stage_bytes<uint16_t>());
-  const int key = f32 ? kSetupSimpleF32 : kSetupSimpleBf16;  // the attribute is the device's
-  if (!setup_done(device, key)) {
-    e = f32 ? cudaFuncSetAttribute(ring_simple_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   max_stages<float>() * stage_bytes<float>())
-            : cudaFuncSetAttribute(ring_simple_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   max_stages<uint16_t>() * stage_bytes<uint16_t>());
-    if (e != cudaSuccess) return e;
-    mark_setup_done(device, key);
-  }
+  // The workers' stores are bound by their SM's store rate: when twice the
+  // grid fits one block per SM, two blocks per (rank, channel) each move a
+  // part of every slice on twice the SMs.
+  const int64_t first_chunk = loop_chunk_count(a.geo, imin(a.geo.per_channel, a.geo.count));
+  const bool split = 2 * grid <= sms && first_chunk >= kSimpleSplitMinChunk;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -598,11 +650,11 @@ cudaError_t launch_ring_simple(const RingArgs& a, int grid, cudaStream_t stream,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (threads_out) *threads_out = kSimpleThreads;
-  if (trace_on())
-    std::fprintf(stderr, "rar trace:   kernel ring_simple_kernel<%s> grid %d threads %d stages %d smem %d\n",
-                 f32 ? "float" : "bf16", grid, kSimpleThreads, nstages, smem);
-  if (f32) return cudaLaunchKernelEx(&cfg, ring_simple_kernel<float>, a, nstages);
-  return cudaLaunchKernelEx(&cfg, ring_simple_kernel<uint16_t>, a, nstages);
+  if (f32)
+    return split ? launch_simple_form<float, 2>(a, cfg, device, nstages, smem, kSetupSimpleF32Split)
+                 : launch_simple_form<float, 1>(a, cfg, device, nstages, smem, kSetupSimpleF32);
+  return split ? launch_simple_form<uint16_t, 2>(a, cfg, device, nstages, smem, kSetupSimpleBf16Split)
+               : launch_simple_form<uint16_t, 1>(a, cfg, device, nstages, smem, kSetupSimpleBf16);
 }
 
 }  // namespace rar

@@ -105,7 +105,7 @@ def test_direct_64MiB_full():
                                         count, bs, 4)
         got = y[0, a:b].cpu().numpy()
         assert got.tobytes() == want.tobytes(), f"mismatch in [{a}, {b})"
-        assert not violations(xs, got, "f32")[0].any()
+        assert not violations(xs, got, "f32").bad.any()
 
 
 def _random_default_buffer_case(seed):
@@ -129,3 +129,17 @@ def test_random_default_buffers(seed):
     or one per channel, sizes from 1 element to 2 Mi, in place or not."""
     n, rings, mask, proto, count, dtype, in_place = _random_default_buffer_case(seed)
     run_ex(n, rings, mask, proto, count, dtype, 0, 4, seed=seed, in_place=in_place)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_direct_split_over_two_blocks(dtype):
+    """The direct all-gather mode with the Simple kernel split over two
+    blocks per (rank, channel) (N=4, 2 channels, one ring per channel, 1 MiB
+    FIFO: 131072-element chunks): calls of changing size on one workspace,
+    direct and FIFO calls alternating, ragged last loops."""
+    n, mask, bs = 4, 0b11, 1 << 20
+    rings = [[0, 2, 3, 1], [0, 1, 2, 3]]
+    loop = n * 131072 * 2
+    ws = None
+    for k, (count, direct) in enumerate([(2 * loop + 999, True), (loop, False), (3000, True), (3 * loop + 5, True)]):
+        ws = run_ex(n, rings, mask, "Simple", count, dtype, bs, 4, direct=direct, seed=350 + k, ws=ws)

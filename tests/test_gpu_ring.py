@@ -65,8 +65,7 @@ def assert_bit_exact(got, want_rows):
 def assert_naive_bound(x, got, dtype, offset=0):
     """Every rank's result within the naive left-to-right sum's bound."""
     for r in range(got.shape[0]):
-        bad, _ = violations(x, got[r], dtype)
-        idx = np.nonzero(bad)[0]
+        idx = np.nonzero(violations(x, got[r], dtype).bad)[0]
         assert idx.size == 0, f"rank {r}: {idx.size} elements outside the naive-sum bound, first at {idx[:8] + offset}"
 
 
@@ -202,9 +201,9 @@ def check_full(case, x, out_row, span=1 << 23):
         bits = np.uint32 if case.dtype == "f32" else np.uint16
         bad = np.nonzero(got.view(bits) != want.view(bits))[0]
         assert bad.size == 0, f"{bad.size} mismatches in [{a}, {b}), first at {bad[:8] + a}"
-        viol, w = violations(xs, got, case.dtype)
-        wide += w
-        idx = np.nonzero(viol)[0]
+        chk = violations(xs, got, case.dtype)
+        wide += chk.wide
+        idx = np.nonzero(chk.bad)[0]
         assert idx.size == 0, f"{idx.size} elements outside the naive-sum bound, first at {idx[:8] + a}"
     return wide
 
@@ -461,6 +460,32 @@ def test_line_bulk_steps_of_changing_size(proto, chunk, n, mask, ring, dtype):
     loop = n * chunk * bin(mask).count("1")
     for k, count in enumerate([10 * loop + 1234, 700, 3 * loop + 7, 25, 2 * loop - 5]):
         case = gen.RingCase("linesplit", n, ring, mask, proto, count, dtype, "normal", 320 + k, 65536, 4)
+        x = case.inputs()
+        want = oracle_full(case, x)
+        _, got, _ = run_ring(case, x=x, workspace=ws, in_place=(k == 4))
+        assert_bit_exact(got, want)
+        assert_naive_bound(x, got, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cs", [4, 2])
+@pytest.mark.parametrize("n,mask,ring", [(4, 0b1, [0, 2, 3, 1]), (3, 0b101, [2, 0, 1])])
+def test_simple_split_slices_of_changing_size(n, mask, ring, cs, dtype):
+    """The Simple kernel split over two blocks per (rank, channel) (grids
+    that fit the SMs twice, first-loop chunks of at least 65536 elements):
+    each part moves a fixed element range of every slice and publishes its
+    own tail; the split point follows the slice's size, so FIFO slots are
+    reused by slices of different sizes (full chunks, the short last loop)
+    and a sender takes a slot only once both receiver parts released it.
+    1 MiB buffers (131072- or 65536-element chunks, one or two steps per
+    slice); split and unsplit calls alternate on one workspace (the step
+    counters carry over), the last in place."""
+    bs = 1 << 20
+    ws = B.Workspace(n, mask, "Simple", bs)
+    chunk = bs // 8 * cs // 4
+    loop = n * chunk * bin(mask).count("1")
+    for k, count in enumerate([3 * loop + 12345, 5000, 2 * loop + 7, 100, loop]):
+        case = gen.RingCase("simplesplit", n, ring, mask, "Simple", count, dtype, "normal", 340 + k, bs, cs)
         x = case.inputs()
         want = oracle_full(case, x)
         _, got, _ = run_ring(case, x=x, workspace=ws, in_place=(k == 4))

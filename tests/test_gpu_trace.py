@@ -1,8 +1,9 @@
 """RAR_TRACE on the GPU: each call names the kernel form it launched, and the
 form follows the first-loop chunk thresholds (LL bulk from 1024 elements,
 LL128 bulk from 960, the polling forms below); the calls stay bit-exact.
-LL128's bulk form splits every (rank, channel) over two blocks when twice the
-grid fits the SMs, and the trace says so."""
+LL128's bulk form and the Simple kernel (large chunks) split every (rank,
+channel) over two blocks when twice the grid fits the SMs, and the trace says
+so."""
 import os
 import re
 import subprocess
@@ -66,14 +67,18 @@ def test_trace_names_the_kernel_form():
         assert re.search(pat, line), (line, pat)
 
 
-def test_trace_reports_the_bulk_split():
+def test_trace_reports_the_split():
     """LL128's bulk form: 4 ranks on 1 channel and 8 ranks on the sparse
     8-channel mask (64 blocks) split; 8 ranks on 12 channels (96 blocks: 192
-    do not fit 152 SMs) do not. LL's bulk form never splits."""
+    do not fit 152 SMs) do not. LL's bulk form never splits. Simple splits a
+    grid that fits twice from first-loop chunks of 65536 elements."""
     cases = [(4, 4 * 2000, "LL128", "f32", 0x1), (8, 8 * 8 * 2000 + 13, "LL128", "bf16", 0b101101011011),
              (8, 8 * 12 * 2000, "LL128", "f32", 0xFFF), (4, 4 * 2048, "LL", "f32", 0x1),
-             (8, 8 * 12 * 2048, "LL", "bf16", 0xFFF)]
-    want = [(r"grid 8 ", "split 2"), (r"grid 128 ", "split 2"), (r"grid 96 ", "split 1"), (r"grid 4 ", "split 1"),
-            (r"grid 96 ", "split 1")]
-    for line, (grid, split) in zip(_kernel_lines(cases), want):
-        assert "ring_line_bulk_kernel" in line and re.search(grid, line) and line.rstrip().endswith(split), line
+             (8, 8 * 12 * 2048, "LL", "bf16", 0xFFF), (4, 4 * 65536, "Simple", "f32", 0x1),
+             (4, 4 * 65536 - 64, "Simple", "f32", 0x1), (8, 8 * 12 * 65536, "Simple", "bf16", 0xFFF)]
+    want = [("ring_line_bulk_kernel", r"grid 8 ", "split 2"), ("ring_line_bulk_kernel", r"grid 128 ", "split 2"),
+            ("ring_line_bulk_kernel", r"grid 96 ", "split 1"), ("ring_line_bulk_kernel", r"grid 4 ", "split 1"),
+            ("ring_line_bulk_kernel", r"grid 96 ", "split 1"), ("ring_simple_kernel", r"grid 8 ", "split 2"),
+            ("ring_simple_kernel", r"grid 4 ", "split 1"), ("ring_simple_kernel", r"grid 96 ", "split 1")]
+    for line, (kernel, grid, split) in zip(_kernel_lines(cases), want):
+        assert kernel in line and re.search(grid, line) and line.rstrip().endswith(split), line
