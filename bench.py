@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # headline kernel from one ncu capture of this workload, and a hash of the
 # kernel sources it was captured with: when the sources differ (the kernel
 # changed since the capture) the line reports traffic null.
-TRAFFIC_BYTES_PER_LAUNCH = 1789474048
-TRAFFIC_SOURCES_SHA16 = "9e02fd2a14188441"
+TRAFFIC_BYTES_PER_LAUNCH = 1789786368
+TRAFFIC_SOURCES_SHA16 = "c27d2b349b90b797"
 TRAFFIC_SOURCES = ("ring_simple.cu", "rar_device.cuh", "rar_geometry.h")
 
 

@@ -1506,6 +1506,7 @@ __device__ __forceinline__ int l8_tiles_ready_f(const RingArgs& a, const char* r
 // boundary whichever type a row's lines carry, and a row's received and sent
 // lines of one part cover the same elements.
 constexpr int kSplitAlign = 240;
+constexpr int64_t kL8SplitMinChunk = kL8TileElems;  // first-loop chunks that split (one whole tile)
 
 template <typename T, int PROTO, int SPLIT>
 __global__ void __launch_bounds__(kL8Threads, 1) ring_line_bulk_kernel(const __grid_constant__ RingArgs a,
@@ -1875,12 +1876,16 @@ cudaError_t launch_ring_line(const RingArgs& a, int grid, cudaStream_t stream, i
   // LL128: the bulk form from 960-element chunks, the polling form (lowest
   // latency) for smaller messages.
   // Two blocks per (rank, channel), each a fixed half of every step, when
-  // twice the grid still fits one block per SM: the bulk form is bound by
-  // its blocks' instruction issue, and a mask of few channels leaves SMs idle
-  // (not in the flag-wrap test mode, whose slot cleanup lives in the polling
-  // form anyway).
+  // twice the grid still fits one block per SM and a step holds at least one
+  // whole tile: the bulk form is bound by its blocks' instruction issue, and
+  // a mask of few channels leaves SMs idle; smaller steps are bound by their
+  // hand-off chain, which a split only lengthens (measured: 512 KiB per rank
+  // on 4 ranks and 12 channels, 2732-element chunks, 19.0 against 17.5 us).
+  // Not in the flag-wrap test mode, whose slot cleanup lives in the polling
+  // form anyway.
   if (first_chunk >= kL8BulkMinChunk && grid <= sms) {
-    if (2 * grid <= sms && a.ll_flag_max == 0) return launch_bulk<kLL128, 2>(a, cfg, f32, device, threads_out);
+    if (2 * grid <= sms && first_chunk >= kL8SplitMinChunk && a.ll_flag_max == 0)
+      return launch_bulk<kLL128, 2>(a, cfg, f32, device, threads_out);
     return launch_bulk<kLL128, 1>(a, cfg, f32, device, threads_out);
   }
   cfg.blockDim = dim3(kThreadsSmall);

@@ -444,22 +444,23 @@ def test_ll_polling_one_pass_of_1024_threads(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("n,mask,ring", [(4, 0b1, [0, 2, 3, 1]), (2, 0b10, [1, 0]), (8, 0b101101011011, None)])
-@pytest.mark.parametrize("proto,chunk", [("LL128", 1920), ("LL", 1024)])
+@pytest.mark.parametrize("proto,chunk", [("LL128", 15360), ("LL", 8192)])
 def test_line_bulk_steps_of_changing_size(proto, chunk, n, mask, ring, dtype):
     """LL128's bulk form split over two blocks per (rank, channel) (grids
     that fit the SMs twice): each half moves a fixed element range of every
     step, and the split point follows the step's size, so FIFO slots are
     reused by steps of different sizes (full chunks, the short last loop, the
     other calls') and a sender writes a slot only once both receiver halves
-    released it. LL's bulk form (one block per pair) on the same calls. 64 KiB
-    buffers (chunks of 1920 LL128 / 1024 LL elements): many loops per channel;
-    calls of different sizes on one workspace, polling-form calls between
-    them, the last in place."""
+    released it. LL's bulk form (one block per pair) on the same calls. 512 KiB
+    buffers (chunks of 15360 LL128 / 8192 LL elements): several loops per
+    channel, each slot reused several times; calls of different sizes on one
+    workspace, polling-form calls between them, the last in place."""
     ring = ring or gen.ring_permutation(n, 47)
-    ws = B.Workspace(n, mask, proto, 65536)
+    bs = 512 << 10
+    ws = B.Workspace(n, mask, proto, bs)
     loop = n * chunk * bin(mask).count("1")
-    for k, count in enumerate([10 * loop + 1234, 700, 3 * loop + 7, 25, 2 * loop - 5]):
-        case = gen.RingCase("linesplit", n, ring, mask, proto, count, dtype, "normal", 320 + k, 65536, 4)
+    for k, count in enumerate([3 * loop + 1234, 700, 2 * loop + 7, 25, loop - 5]):
+        case = gen.RingCase("linesplit", n, ring, mask, proto, count, dtype, "normal", 320 + k, bs, 4)
         x = case.inputs()
         want = oracle_full(case, x)
         _, got, _ = run_ring(case, x=x, workspace=ws, in_place=(k == 4))

@@ -68,17 +68,21 @@ def test_trace_names_the_kernel_form():
 
 
 def test_trace_reports_the_split():
-    """LL128's bulk form: 4 ranks on 1 channel and 8 ranks on the sparse
-    8-channel mask (64 blocks) split; 8 ranks on 12 channels (96 blocks: 192
-    do not fit 152 SMs) do not. LL's bulk form never splits. Simple splits a
-    grid that fits twice from first-loop chunks of 65536 elements."""
-    cases = [(4, 4 * 2000, "LL128", "f32", 0x1), (8, 8 * 8 * 2000 + 13, "LL128", "bf16", 0b101101011011),
-             (8, 8 * 12 * 2000, "LL128", "f32", 0xFFF), (4, 4 * 2048, "LL", "f32", 0x1),
+    """LL128's bulk form (first-loop chunks of 8000 elements, at least one
+    whole tile): 4 ranks on 1 channel and 8 ranks on the sparse 8-channel mask
+    (64 blocks) split; 8 ranks on 12 channels (96 blocks: 192 do not fit 152
+    SMs) do not; 2000-element chunks do not. LL's bulk form never splits.
+    Simple splits a grid that fits twice from first-loop chunks of 65536
+    elements."""
+    cases = [(4, 4 * 8000, "LL128", "f32", 0x1), (8, 8 * 8 * 8000 + 13, "LL128", "bf16", 0b101101011011),
+             (8, 8 * 12 * 8000, "LL128", "f32", 0xFFF), (4, 4 * 2048, "LL", "f32", 0x1),
              (8, 8 * 12 * 2048, "LL", "bf16", 0xFFF), (4, 4 * 65536, "Simple", "f32", 0x1),
-             (4, 4 * 65536 - 64, "Simple", "f32", 0x1), (8, 8 * 12 * 65536, "Simple", "bf16", 0xFFF)]
+             (4, 4 * 65536 - 64, "Simple", "f32", 0x1), (8, 8 * 12 * 65536, "Simple", "bf16", 0xFFF),
+             (4, 4 * 2000, "LL128", "f32", 0x1)]
     want = [("ring_line_bulk_kernel", r"grid 8 ", "split 2"), ("ring_line_bulk_kernel", r"grid 128 ", "split 2"),
             ("ring_line_bulk_kernel", r"grid 96 ", "split 1"), ("ring_line_bulk_kernel", r"grid 4 ", "split 1"),
             ("ring_line_bulk_kernel", r"grid 96 ", "split 1"), ("ring_simple_kernel", r"grid 8 ", "split 2"),
-            ("ring_simple_kernel", r"grid 4 ", "split 1"), ("ring_simple_kernel", r"grid 96 ", "split 1")]
+            ("ring_simple_kernel", r"grid 4 ", "split 1"), ("ring_simple_kernel", r"grid 96 ", "split 1"),
+            ("ring_line_bulk_kernel", r"grid 4 ", "split 1")]
     for line, (kernel, grid, split) in zip(_kernel_lines(cases), want):
         assert kernel in line and re.search(grid, line) and line.rstrip().endswith(split), line
