@@ -3,7 +3,9 @@
  *
  * N "virtual ranks" live in one GPU: every rank's send buffer, receive buffer
  * and connector FIFOs are ordinary device memory of that GPU, and one kernel
- * launch runs all ranks at once (one thread block per (rank, channel)).
+ * launch runs all ranks at once (one thread block per (rank, channel); for
+ * large Simple and LL128 messages two blocks per (rank, channel), each moving
+ * a fixed part of every step, when twice the grid fits the device's SMs).
  *
  * Pages the operations follow (cited by title and section):
  *   [C23] "NCCL 专家课程 23：Device Kernel、Primitives、Step/Credit 与 LL Flag"
@@ -76,7 +78,8 @@ typedef enum rar_proto { RAR_LL = 0, RAR_LL128 = 1, RAR_SIMPLE = 2 } rar_proto;
  * buffSize 0 selects the protocol's default (Simple 4 MiB, LL 512 KiB,
  * LL128 4915200 bytes). Layout: a 4 KiB header (status word, abort flag, the
  * configuration it was initialised for, a per-block trace), then a 256-byte
- * head/tail record per connection, then one FIFO of buffSize bytes per
+ * head/tail record per connection (with a second head/tail pair for the
+ * second part of a two-block launch), then one FIFO of buffSize bytes per
  * connection; a connection is one (channel, ring edge) pair, so there are
  * nranks * popcount(channelMask) of each. Returns 0 for invalid arguments.
  */
