@@ -703,6 +703,9 @@ __global__ void __launch_bounds__(NT, 1) ring_line_kernel(const __grid_constant_
 //                   per 4 lines, flag word included.
 //   warp 2, lane 0  poster: publishes the head once the step's lines are read.
 // A line is accepted only by its own flag, exactly as in the polling form.
+// LL128's split instance (SPLIT = 2) runs two blocks per (rank, channel):
+// each moves a fixed part of every step's elements with the roles above, keeps
+// its own head counter, and takes a slot's credit from both receiver parts.
 // ---------------------------------------------------------------------------
 constexpr int kL8TileElems = 7680;   // 64 groups of binary32 payload, 32 groups of bf16 payload
 constexpr int kL8TileGroups = kL8TileElems * 4 / 480;
