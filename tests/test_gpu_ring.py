@@ -319,7 +319,8 @@ def test_too_many_blocks_is_refused():
 
 
 @pytest.mark.parametrize("proto,count,bs", [("Simple", 200000, 65536), ("LL", 200000, 0), ("LL", 200000, 4096),
-                                           ("LL128", 20000, 65536), ("LL128", 400000, 131072)])
+                                           ("LL128", 20000, 65536), ("LL128", 400000, 131072),
+                                           ("Simple", 600000, 1 << 20), ("LL128", 300000, 524288)])
 def test_dropped_head_times_out_and_recovers(proto, count, bs):
     """Failure detection without a GPU fault: with the receivers' head
     updates dropped, every sender runs out of credit after NCCL_STEPS steps;
@@ -329,7 +330,9 @@ def test_dropped_head_times_out_and_recovers(proto, count, bs):
     sizes give every connection more than NCCL_STEPS steps; the two LL128
     cases use the polling and the bulk form, the LL case with a 4 KiB buffer
     the polling form whose block meets every NCCL_STEPS / 2 steps (the sender
-    then waits for credit at a group boundary)."""
+    then waits for credit at a group boundary); the last Simple and LL128
+    cases split every (rank, channel) over two blocks (first-loop chunks of
+    75000 and 15360 elements), whose senders wait for both receiver parts."""
     case = gen.RingCase("fault", 4, gen.RING_0231, 0b11, proto, count, "f32", "normal", 8, bs, 4)
     x = case.inputs()
     _, send = to_device(x, "f32")
